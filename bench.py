@@ -1,0 +1,398 @@
+"""Benchmark of the ring-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of the 128K causal striped
+workload (B=1, H=8, L=131072, d=128, N=16 virtual ranks): shard Q, K and V
+into the striped ring layout, run the fused ring sweep, and put O and LSE back
+in token order.  Inputs are synthetic (seeded N(0, 1) bf16) and larger than
+L2, so nothing is reused from cache between steps.
+
+The metric is algorithmic TFLOP/s: 4 * B * H * d * L(L+1)/2 flops per step
+(the causal pairs, counted once per layout; skipped and masked work is not
+counted).  Besides the device-resident number the JSON line carries:
+  * roofline  -- the attention kernel alone: its CUDA-event time per launch
+                 against the measured dense-bf16 peak;
+  * e2e       -- the same metric through the same public calls with the step's
+                 inputs copied from pinned host memory and O / LSE copied back;
+  * cpu_baseline -- the fp64 CPU oracle, timed on a bounded sample of query rows;
+  * clocks    -- SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the CPU oracle itself on the same workload and metric.
+Under torchrun (N > 1) every rank runs its own replica of the workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from synthetic_inputs import WORKLOADS, make_qkv  # noqa: E402
+
+METRIC = "causal ring-attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
+DEFAULT_WORKLOAD = "striped_B1_H8_L131072_d128_N16"
+LAUNCHES_PER_STEP = 6          # 3 shard permutes, 1 ring sweep, 1 O un-permute, 1 LSE un-permute
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_striped_128k_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "sequence_blockwise_softmax_gb300", "csrc", f)
+                  for f in ("attn_sm103.cu", "ra_device.cuh")]
+
+
+def algorithmic_flops(B, L, H, d, causal):
+    pairs = L * (L + 1) // 2 if causal else L * L
+    return 4.0 * B * H * d * pairs
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary,
+    or None when the kernel source changed since it was taken."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    key, val = line.split(":", 1)
+                    fields[key.strip()] = val.strip()
+        if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_full_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "-i", str(self.index),
+               "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                bits = int(parts[3], 16)
+            except ValueError:
+                continue
+            for bit, name in REASON_BITS.items():
+                if bits & bit and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- the GPU path
+class Workload:
+    def __init__(self, ra, name, layout, dev):
+        w = WORKLOADS[name]
+        self.ra, self.name, self.layout, self.dev = ra, name, layout, dev
+        self.B, self.L, self.H, self.d, self.N = w["B"], w["L"], w["H"], w["d"], w["N"]
+        self.U = w.get("U", 1)
+        self.causal = w["causal"]
+        B, L, H, d, N, U = self.B, self.L, self.H, self.d, self.N, self.U
+        q, k, v, _ = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])
+        self.host = [t.pin_memory() for t in (q, k, v)]
+        self.seq = [t.to(dev) for t in self.host]
+        P = U * N
+        self.shard = [torch.empty((P, B, L // P, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        if U > 1:
+            self.head = [torch.empty((N, U, B, L // N, H // U, d), dtype=torch.bfloat16, device=dev)
+                         for _ in range(3)]
+        self.Bq, self.Hq = U * B, H // U
+        ring_in = self.head if U > 1 else self.shard
+        self.o_ring = torch.empty_like(ring_in[0])
+        self.lse_ring = torch.empty((N, self.Bq, self.Hq, L // N), dtype=torch.float32, device=dev)
+        self.o_shard = torch.empty_like(self.shard[0]) if U > 1 else None
+        self.o_seq = torch.empty((B, L, H, d), dtype=torch.bfloat16, device=dev)
+        self.lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+        self.o_host = torch.empty((B, L, H, d), dtype=torch.bfloat16).pin_memory()
+        self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
+        self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N), device=dev)
+        self.flops = algorithmic_flops(B, L, H, d, self.causal)
+        self.launches = 3 * (2 if U > 1 else 1) + 1 + (2 if U > 1 else 1) + 1
+        self.attn_events = []
+
+    def step(self, time_attention=False):
+        ra, B, L, H, d, N, U = self.ra, self.B, self.L, self.H, self.d, self.N, self.U
+        for i in range(3):
+            ra.ra_shard_permute(self.seq[i], self.shard[i], ra.RA_SEQ_TO_SHARDS, self.layout, B, L, H, d, N, U)
+            if U > 1:
+                ra.ra_shard_permute(self.shard[i], self.head[i], ra.RA_ULYSSES_SEQ_TO_HEAD, self.layout,
+                                    B, L, H, d, N, U)
+        ring_in = self.head if U > 1 else self.shard
+        if time_attention:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        ra.ra_ring_attn_fwd(*ring_in, self.o_ring, self.lse_ring, self.Bq, L, self.Hq, d, N, self.layout,
+                            self.causal, workspace=self.ws)
+        if time_attention:
+            e1.record()
+            self.attn_events.append((e0, e1))
+        o = self.o_ring
+        if U > 1:
+            ra.ra_shard_permute(o, self.o_shard, ra.RA_ULYSSES_HEAD_TO_SEQ, self.layout, B, L, H, d, N, U)
+            o = self.o_shard
+        ra.ra_shard_permute(o, self.o_seq, ra.RA_SHARDS_TO_SEQ, self.layout, B, L, H, d, N, U)
+        ra.ra_lse_to_seq(self.lse_ring, self.lse_seq, self.layout, B, L, H, N, U)
+
+    def step_e2e(self):
+        for h, s in zip(self.host, self.seq):
+            s.copy_(h, non_blocking=True)
+        self.step()
+        self.o_host.copy_(self.o_seq, non_blocking=True)
+        self.lse_host.copy_(self.lse_seq, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host)
+
+    def d2h_bytes(self):
+        return self.o_host.numel() * 2 + self.lse_host.numel() * 4
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed(fn, steps, world, dev):
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+def oracle_sample_run(name, budget_s, seed=0, cache={}):
+    """Time the fp64 oracle on a random sample of query rows (all batches and heads)
+    sized to about ``budget_s`` seconds.  Returns (flops, seconds, rows, threads)."""
+    import oracle
+    w = WORKLOADS[name]
+    B, L, H, d = w["B"], w["L"], w["H"], w["d"]
+    key = (name,)
+    if key not in cache:
+        cache[key] = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])[:3]
+    q, k, v = cache[key]
+    rng = np.random.default_rng(seed)
+
+    def run(n):
+        rows = np.sort(rng.integers(0, L, n))
+        t0 = time.perf_counter()
+        oracle.full_attention(q, k, v, causal=w["causal"], rows=rows)
+        dt = time.perf_counter() - t0
+        keys = (rows + 1).sum() if w["causal"] else n * L
+        return 4.0 * B * H * d * float(keys), dt, n
+
+    fl, dt, n = run(4)                       # calibration
+    rate = fl / max(dt, 1e-6)
+    per_row = 4.0 * B * H * d * (L / 2 if w["causal"] else L)
+    n = max(4, int(budget_s * rate / per_row))
+    fl, dt, n = run(n)
+    return fl, dt, n, oracle.num_threads()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    name = args.workload
+    w = WORKLOADS[name]
+    layout = args.layout or w["layouts"][0]
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_sample_run(name, per_step, seed=100 + i)
+    fl_tot, t_tot, rows_tot, threads = 0.0, 0.0, 0, 1
+    for i in range(args.steps):
+        fl, dt, n, threads = oracle_sample_run(name, per_step, seed=i)
+        fl_tot += fl
+        t_tot += dt
+        rows_tot += n
+    value = fl_tot / t_tot / 1e12
+    sample = ("%d random query rows (all %d heads) of the %s workload, %d steps of ~%.0f s"
+              % (rows_tot, w["H"], name, args.steps, per_step))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": name, "layout": layout, "B": w["B"], "L": w["L"], "H": w["H"],
+                   "d": w["d"], "N": w["N"], "causal": w["causal"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--layout", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import sequence_blockwise_softmax_gb300 as ra
+    ra.lib()  # fails loudly when the library is missing
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+
+    w = WORKLOADS[args.workload]
+    layout = args.layout or w["layouts"][0]
+    wl = Workload(ra, args.workload, layout, dev)
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    ra.ra_check_status(wl.ws)
+
+    # device-resident timed region
+    wl.attn_events = []
+    with ClockSampler(local_rank) as clocks:
+        ms = timed(lambda: wl.step(time_attention=True), args.steps, world, dev)
+    ms_step = ms / args.steps
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in wl.attn_events]))
+    attn_ms = max_over_ranks(attn_ms, world, dev)
+    ra.ra_check_status(wl.ws)
+
+    # end to end through the same calls, host buffers in and out
+    for _ in range(2):
+        wl.step_e2e()
+    ms_e2e = timed(wl.step_e2e, args.steps, world, dev) / args.steps
+    ra.ra_check_status(wl.ws)
+
+    total_flops = wl.flops * world
+    value = total_flops / (ms_step * 1e-3) / 1e12
+    e2e_value = total_flops / (ms_e2e * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = wl.flops / (attn_ms * 1e-3) / 1e12
+    traffic = read_traffic()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
+                   "d": wl.d, "N": wl.N, "U": wl.U, "causal": wl.causal,
+                   "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
+                   "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<128,false> (ra_ring_attn_fwd)",
+                     "kernel_ms": attn_ms,
+                     "peak_source": "%s bf16_tflops_sustained" % peak_src},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),
+                "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": ms_e2e},
+        "gpu_launches": wl.launches * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, dt, n, threads = oracle_sample_run(args.workload, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d random query rows x %d heads of the workload (%.1f s of fp64 work)"
+                      % (n, wl.H, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+/*
+ * ra.h -- C ABI of the GB300 ring-attention library (libra_gb300.so).
+ *
+ * Exact blockwise attention, softmax(Q K^T / sqrt(d)) V, over a sequence
+ * split into N shards ("virtual ranks") that all live on ONE GPU.  Each query
+ * shard is swept over the key/value shards in ring order and the partial
+ * results are combined with the online-softmax merge; the causal mask is
+ * decided from global token positions.  Sources (page title, section):
+ *   [USP]  "From Ring Attention to DeepSpeed Ulysses to USP"
+ *          (jsqmd.com/news/734632): §2 attention, §3.1 ring order,
+ *          §3.2 online softmax, §3.4 causal imbalance, §4 striped,
+ *          §5.1 Ulysses, §6.1 zigzag, §6.3 LSE merge, §7.1-7.2 USP.
+ *   [SPQ]  "What problem does sequence parallelism solve?"
+ *          (model.playoffer.cn, sequence-parallelism): engineering notes
+ *          (the ring decides the causal mask by position).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates device memory and keeps no pointer after a call returns.
+ *   - Every pointer must be 16-byte aligned (RA_ERR_ALIGNMENT otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous and stream-ordered.
+ *   - Arguments are checked on the host before anything is launched; a failed
+ *     check returns a status and launches nothing.  ra_last_error() then gives
+ *     a message (per host thread).
+ *   - A launch failure returns RA_ERR_CUDA.
+ *   - Every wait inside the attention kernels is bounded (about two seconds);
+ *     a kernel that gives up records RA_ERR_TIMEOUT in the status word at the
+ *     start of `workspace`, releases what it holds and exits.
+ *     ra_check_status() reports and clears it.
+ *   - Tensors are row-major.  Full-sequence tensors are [B, L, H, d] (the
+ *     pages' [bs, seq, heads, head_dim]); a stack of N shards is
+ *     [N, B, S, H, d] with S = L / N; LSE tensors are fp32 [.., H, S] in
+ *     natural log.
+ */
+#ifndef RA_GB300_H
+#define RA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RA_API __attribute__((visibility("default")))
+#else
+#define RA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, bad flag, bad scale        */
+    RA_ERR_SHAPE = 2,        /* sizes that do not divide as the layout needs       */
+    RA_ERR_UNSUPPORTED = 3,  /* a valid request this build does not implement      */
+    RA_ERR_ALIGNMENT = 4,    /* a pointer or row that is not 16-byte aligned       */
+    RA_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed               */
+    RA_ERR_TIMEOUT = 6       /* a kernel gave up on a bounded wait                 */
+} ra_status;
+
+/* Token -> rank assignment.  Rank r, local token s holds global token:
+ *   RA_CONTIGUOUS  r*S + s                                   ([USP] §3.1, §4)
+ *   RA_STRIPED     s*N + r                                   ([USP] §4)
+ *   RA_ZIGZAG      2N chunks of C = S/2 tokens; rank r holds chunks r and
+ *                  2N-1-r in that order: s < C -> r*C + s,
+ *                  s >= C -> (2N-1-r)*C + (s - C)            ([USP] §6.1)   */
+typedef enum { RA_CONTIGUOUS = 0, RA_STRIPED = 1, RA_ZIGZAG = 2 } ra_layout;
+
+typedef enum {
+    RA_SEQ_TO_SHARDS = 0,        /* [B, L, H, d] -> [U*R, B, L/(U*R), H, d]        */
+    RA_SHARDS_TO_SEQ = 1,        /* inverse of RA_SEQ_TO_SHARDS                     */
+    RA_ULYSSES_SEQ_TO_HEAD = 2,  /* [U*R, B, L/(U*R), H, d] -> [R, U, B, L/R, H/U, d] */
+    RA_ULYSSES_HEAD_TO_SEQ = 3   /* inverse of RA_ULYSSES_SEQ_TO_HEAD               */
+} ra_perm_op;
+
+/* ra_ring_attn_fwd flags */
+#define RA_FLAG_STEPWISE 1u  /* run the sweep as N x (block attention + LSE merge) */
+
+/* Smallest workspace any attention call accepts (the status word and padding). */
+#define RA_WORKSPACE_MIN_BYTES 256u
+
+/*
+ * ra_shard_permute -- move tokens between the full sequence and the shard
+ * stacks, and between the sequence-sharded and head-sharded Ulysses states.
+ * Every op is a pure copy (bit-exact), one contiguous run of bytes per token.
+ *
+ * R ring ranks, U Ulysses ranks, P = U*R virtual ranks; global rank
+ * p = u*R + r (row u, column r of the USP grid, [USP] §7.1).  U = 1 gives a
+ * plain ring.
+ *   RA_SEQ_TO_SHARDS: dst[u*R + r][b][s] = src[b][pos(r, u*L/P + s)], where
+ *       pos is `layout` over R ranks of L/R tokens: ring rank r's token list,
+ *       cut into U contiguous pieces ([USP] §7.2 input state [bs, L/N, H, d]).
+ *   RA_ULYSSES_SEQ_TO_HEAD: the all-to-all of [USP] §5.1/§7.2 inside each
+ *       Ulysses group (column r), as a local gather:
+ *       dst[r][u'][b][u*Lp + s][hh] = src[u*R + r][b][s][u'*H/U + hh],
+ *       Lp = L/P.  Block (r, u') is [B, L/R, H/U, d]: ring shard r of head
+ *       group u', so dst viewed as [R, U*B, L/R, H/U, d] is a ring stack that
+ *       one ra_ring_attn_fwd call sweeps.
+ *   The _TO_SEQ / _HEAD_TO_SEQ ops are the exact inverses.
+ * src, dst: device, non-overlapping; element size elem_bytes (1, 2, 4 or 8;
+ * 2 for bf16, 4 for fp32).  Requires P | L, and for zigzag 2R | L; U | H for the Ulysses ops;
+ * (H*d*elem_bytes) and ((H/U)*d*elem_bytes) multiples of 16.
+ */
+RA_API ra_status ra_shard_permute(const void *src, void *dst, int op, int layout,
+                           int64_t B, int64_t L, int64_t H, int64_t d,
+                           int R, int U, int elem_bytes, void *stream);
+
+/*
+ * ra_lse_to_seq -- put a ring call's LSE back in token order.
+ * src: fp32 [R, U*B, H/U, L/R] (the LSE of a ring call on a head-sharded
+ * stack; U = 1 is the plain [N, B, H, S]); dst: fp32 [B, H, L] with
+ * dst[b][u*H/U + hh][pos(r, s)] = src[r][u*B + b][hh][s].  Bit-exact copy.
+ */
+RA_API ra_status ra_lse_to_seq(const float *src, float *dst, int layout, int64_t B, int64_t L,
+                        int64_t H, int R, int U, void *stream);
+
+/*
+ * ra_block_attn_fwd -- one ring step: query shard q_rank against key/value
+ * shard kv_rank ([USP] §3.3 "flash_attn_block", §6.2).
+ * q, k, v: bf16 [B, S, H, d], the two ranks' shards.  Token positions come
+ * from `layout` over N ranks of S tokens; with `causal` a query at position t
+ * sees the keys at positions <= t ([USP] §3.4, [SPQ] engineering notes).
+ * o: fp32 [B, S, H, d], the partial output normalised over the keys this
+ * shard contributes; lse: fp32 [B, H, S], ln of the sum of exp(score) over
+ * them.  A row that sees no key of this shard gets o = 0, lse = -inf.
+ * scale <= 0 selects 1/sqrt(d).  d is 64 or 128; workspace: device, at least
+ * RA_WORKSPACE_MIN_BYTES, zero-filled before its first use (status word).
+ */
+RA_API ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *o, float *lse,
+                            int64_t B, int64_t S, int64_t H, int d, int N, int q_rank,
+                            int kv_rank, int layout, int causal, float scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ra_lse_merge -- fold partial result b into accumulator acc, in place
+ * ([USP] §6.3):  lse = max(lse_a, lse_b) + ln(1 + exp(-|lse_a - lse_b|)),
+ *                O   = O_a exp(lse_a - lse) + O_b exp(lse_b - lse).
+ * o_acc, o_b: fp32 [B, S, H, d]; lse_acc, lse_b: fp32 [B, H, S].
+ * -inf marks an empty partial: it gets weight 0, and two empty partials stay
+ * (O = 0, lse = -inf).  d is a multiple of 4, at most 256.
+ */
+RA_API ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
+                       int64_t B, int64_t S, int64_t H, int d, void *stream);
+
+/*
+ * ra_ring_attn_fwd -- the whole ring sweep ([USP] §3.1-§3.3): for every rank
+ * i and step s = 0..N-1, query shard i meets key/value shard (i - s) mod N
+ * and the results are merged online ([USP] §3.2).  All N ranks run at once.
+ * q, k, v: bf16 [N, B, S, H, d] shard stacks (S = L / N) in `layout`;
+ * o: bf16 [N, B, S, H, d]; lse: fp32 [N, B, H, S] (natural log).
+ * Requires N | L, 2N | L for zigzag, d in {64, 128}.  scale <= 0 selects
+ * 1/sqrt(d).  flags: 0 (fused sweep) or RA_FLAG_STEPWISE.  workspace: device,
+ * ra_ring_attn_workspace_bytes() bytes, zero-filled before its first use.
+ */
+RA_API ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t L, int64_t H, int d, int N, int layout,
+                           int causal, float scale, unsigned flags,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes ra_ring_attn_fwd needs for these arguments (0 on bad ones). */
+RA_API size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N,
+                                    unsigned flags);
+
+/*
+ * ra_check_status -- synchronise `stream`, read the status word at the start
+ * of `workspace`, clear it, and return RA_ERR_TIMEOUT if a kernel recorded a
+ * timeout since the last check (RA_OK otherwise).
+ */
+RA_API ra_status ra_check_status(void *workspace, void *stream);
+
+/* Message for the last non-OK status returned on this host thread. */
+RA_API const char *ra_last_error(void);
+
+/* Library version string. */
+RA_API const char *ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RA_GB300_H */

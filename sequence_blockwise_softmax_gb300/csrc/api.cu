@@ -1,0 +1,264 @@
+// api.cu -- the C ABI (include/ra.h): argument checks, workspace layout and
+// launch order.  Every check runs on the host before any CUDA call, so a
+// rejected call touches neither the device nor the stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "ra_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ra_status fail(ra_status st, const std::string &msg) {
+    g_last_error = msg;
+    return st;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_layout(int layout) {
+    return layout == RA_CONTIGUOUS || layout == RA_STRIPED || layout == RA_ZIGZAG;
+}
+
+// Workspace layout: [0, 256) status word + reserved; then, for the stepwise
+// sweep, the fp32 output accumulator and one fp32 partial (O and LSE), each
+// starting on a 256-byte boundary.
+constexpr size_t kHeader = RA_WORKSPACE_MIN_BYTES;
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct StepwiseLayout {
+    size_t o_acc, o_part, lse_part, total;
+};
+
+StepwiseLayout stepwise_layout(int64_t B, int64_t L, int64_t H, int d, int N) {
+    const size_t n_o = (size_t)B * (size_t)L * (size_t)H * (size_t)d;  // N*B*S*H*d
+    const size_t n_lse = (size_t)B * (size_t)L * (size_t)H;
+    (void)N;
+    StepwiseLayout s;
+    s.o_acc = kHeader;
+    s.o_part = s.o_acc + round256(n_o * 4);
+    s.lse_part = s.o_part + round256(n_o * 4);
+    s.total = s.lse_part + round256(n_lse * 4);
+    return s;
+}
+
+ra_status check_attn_common(int64_t B, int64_t S, int64_t H, int d, int N, int layout, float scale) {
+    if (B < 0 || S < 0 || H < 0) return fail(RA_ERR_SHAPE, "B, S and H must be non-negative");
+    if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
+    if (!valid_layout(layout)) return fail(RA_ERR_INVALID_ARG, "layout must be RA_CONTIGUOUS, RA_STRIPED or RA_ZIGZAG");
+    if (d != 64 && d != 128) return fail(RA_ERR_UNSUPPORTED, "head dimension d must be 64 or 128");
+    if (std::isnan(scale) || std::isinf(scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite");
+    if (layout == RA_ZIGZAG && (S % 2) != 0)
+        return fail(RA_ERR_SHAPE, "zigzag needs an even shard length (2N | L)");
+    if (S > (int64_t)1 << 30 || H > (int64_t)1 << 20 || B > (int64_t)1 << 20)
+        return fail(RA_ERR_UNSUPPORTED, "B, S or H beyond the supported range");
+    if ((int64_t)N * B > (int64_t)1 << 30)
+        return fail(RA_ERR_UNSUPPORTED, "N * B beyond the supported range");
+    if (S * H * d * 2 >= ((int64_t)1 << 40))
+        return fail(RA_ERR_UNSUPPORTED, "one shard exceeds the 2^40-byte tensor-map stride limit");
+    return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ra_last_error(void) { return g_last_error.c_str(); }
+
+const char *ra_version(void) { return "ra_gb300 0.1 (sm_103a)"; }
+
+ra_status ra_shard_permute(const void *src, void *dst, int op, int layout, int64_t B, int64_t L,
+                           int64_t H, int64_t d, int R, int U, int elem_bytes, void *stream) {
+    if (op < RA_SEQ_TO_SHARDS || op > RA_ULYSSES_HEAD_TO_SEQ)
+        return fail(RA_ERR_INVALID_ARG, "unknown permute op");
+    if (!valid_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout");
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return fail(RA_ERR_INVALID_ARG, "elem_bytes must be 1, 2, 4 or 8");
+    if (B < 0 || L < 0 || H < 0 || d < 0) return fail(RA_ERR_SHAPE, "sizes must be non-negative");
+    if (R < 1 || U < 1) return fail(RA_ERR_SHAPE, "R and U must be at least 1");
+    const int64_t P = (int64_t)R * U;
+    if (L % P) return fail(RA_ERR_SHAPE, "U*R must divide L");
+    if (layout == RA_ZIGZAG && (L % (2 * (int64_t)R)))
+        return fail(RA_ERR_SHAPE, "zigzag needs 2R | L");
+    const bool ulysses = op == RA_ULYSSES_SEQ_TO_HEAD || op == RA_ULYSSES_HEAD_TO_SEQ;
+    if (ulysses && (H % U)) return fail(RA_ERR_SHAPE, "U must divide H");
+    if ((H * d * elem_bytes) % 16)
+        return fail(RA_ERR_ALIGNMENT, "a token's H*d*elem_bytes must be a multiple of 16 bytes");
+    if (ulysses && (((H / U) * d * elem_bytes) % 16))
+        return fail(RA_ERR_ALIGNMENT, "a head slice (H/U)*d*elem_bytes must be a multiple of 16 bytes");
+    if (B * L * H * d == 0) return RA_OK;
+    if (!src || !dst) return fail(RA_ERR_INVALID_ARG, "null src or dst");
+    if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_ALIGNMENT, "src and dst must be 16-byte aligned");
+    if (src == dst) return fail(RA_ERR_INVALID_ARG, "src and dst must not be the same buffer");
+    const char *err = nullptr;
+    ra_status st = ra::launch_permute(src, dst, op, layout, B, L, H, d, R, U, elem_bytes,
+                                      static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "permute launch failed");
+}
+
+ra_status ra_lse_to_seq(const float *src, float *dst, int layout, int64_t B, int64_t L, int64_t H,
+                        int R, int U, void *stream) {
+    if (!valid_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout");
+    if (B < 0 || L < 0 || H < 0) return fail(RA_ERR_SHAPE, "sizes must be non-negative");
+    if (R < 1 || U < 1) return fail(RA_ERR_SHAPE, "R and U must be at least 1");
+    if (L % R) return fail(RA_ERR_SHAPE, "R must divide L");
+    if (layout == RA_ZIGZAG && (L % (2 * (int64_t)R))) return fail(RA_ERR_SHAPE, "zigzag needs 2R | L");
+    if (H % U) return fail(RA_ERR_SHAPE, "U must divide H");
+    if (B * L * H == 0) return RA_OK;
+    if (!src || !dst) return fail(RA_ERR_INVALID_ARG, "null src or dst");
+    if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_ALIGNMENT, "src and dst must be 16-byte aligned");
+    const char *err = nullptr;
+    ra_status st = ra::launch_lse_to_seq(src, dst, layout, B, L, H, R, U,
+                                         static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "lse_to_seq launch failed");
+}
+
+ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *o, float *lse,
+                            int64_t B, int64_t S, int64_t H, int d, int N, int q_rank, int kv_rank,
+                            int layout, int causal, float scale, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
+    if (st != RA_OK) return st;
+    if (q_rank < 0 || q_rank >= N || kv_rank < 0 || kv_rank >= N)
+        return fail(RA_ERR_INVALID_ARG, "q_rank and kv_rank must lie in [0, N)");
+    if (B * S * H == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(workspace))
+        return fail(RA_ERR_ALIGNMENT, "every pointer must be 16-byte aligned");
+    if (workspace_bytes < RA_WORKSPACE_MIN_BYTES)
+        return fail(RA_ERR_INVALID_ARG, "workspace smaller than RA_WORKSPACE_MIN_BYTES");
+    ra::AttnLaunch a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.status = static_cast<unsigned *>(workspace);
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.d = d;
+    a.N = N;
+    a.layout = layout;
+    a.causal = causal;
+    a.scale = scale;
+    a.ring = false;
+    a.q_rank = q_rank;
+    a.kv_rank = kv_rank;
+    a.ring_step = -1;
+    a.out_f32 = true;
+    const char *err = nullptr;
+    st = ra::launch_attention(a, static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "attention launch failed");
+}
+
+ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b, int64_t B,
+                       int64_t S, int64_t H, int d, void *stream) {
+    if (B < 0 || S < 0 || H < 0 || d < 0) return fail(RA_ERR_SHAPE, "sizes must be non-negative");
+    if (d % 4 || d > 256) return fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4, at most 256");
+    if (B * S * H * d == 0) return RA_OK;
+    if (!o_acc || !lse_acc || !o_b || !lse_b) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(o_acc) || !aligned16(lse_acc) || !aligned16(o_b) || !aligned16(lse_b))
+        return fail(RA_ERR_ALIGNMENT, "every pointer must be 16-byte aligned");
+    const char *err = nullptr;
+    ra_status st = ra::launch_lse_merge(o_acc, lse_acc, o_b, lse_b, B, S, H, d,
+                                        static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "merge launch failed");
+}
+
+size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N, unsigned flags) {
+    if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
+    if (flags & RA_FLAG_STEPWISE) return stepwise_layout(B, L, H, d, N).total;
+    return kHeader;
+}
+
+ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t L, int64_t H, int d, int N, int layout, int causal,
+                           float scale, unsigned flags, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    if (flags & ~RA_FLAG_STEPWISE) return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
+    if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
+    if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
+    if (L % N) return fail(RA_ERR_SHAPE, "N must divide L");
+    if (layout == RA_ZIGZAG && (L % (2 * (int64_t)N))) return fail(RA_ERR_SHAPE, "zigzag needs 2N | L");
+    const int64_t S = L / N;
+    ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
+    if (st != RA_OK) return st;
+    if (B * L * H == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(workspace))
+        return fail(RA_ERR_ALIGNMENT, "every pointer must be 16-byte aligned");
+    const size_t need = ra_ring_attn_workspace_bytes(B, L, H, d, N, flags);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace smaller than ra_ring_attn_workspace_bytes()");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char *err = nullptr;
+    ra::AttnLaunch a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.lse = lse;
+    a.status = static_cast<unsigned *>(workspace);
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.d = d;
+    a.N = N;
+    a.layout = layout;
+    a.causal = causal;
+    a.scale = scale;
+    a.ring = true;
+    if (!(flags & RA_FLAG_STEPWISE)) {
+        a.o = o;
+        a.ring_step = -1;
+        a.out_f32 = false;
+        st = ra::launch_attention(a, s, &err);
+        return st == RA_OK ? st : fail(st, err ? err : "attention launch failed");
+    }
+    // Stepwise: the pages' per-step structure -- at step s every rank meets
+    // KV shard (i - s) mod N, then the partial result is merged in.
+    StepwiseLayout wl = stepwise_layout(B, L, H, d, N);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *o_acc = reinterpret_cast<float *>(ws + wl.o_acc);
+    float *o_part = reinterpret_cast<float *>(ws + wl.o_part);
+    float *lse_part = reinterpret_cast<float *>(ws + wl.lse_part);
+    a.out_f32 = true;
+    for (int step = 0; step < N; ++step) {
+        a.ring_step = step;
+        a.o = step == 0 ? o_acc : o_part;
+        a.lse = step == 0 ? lse : lse_part;
+        st = ra::launch_attention(a, s, &err);
+        if (st != RA_OK) return fail(st, err ? err : "attention launch failed");
+        if (step > 0) {
+            st = ra::launch_lse_merge(o_acc, lse, o_part, lse_part, (int64_t)N * B, S, H, d, s, &err);
+            if (st != RA_OK) return fail(st, err ? err : "merge launch failed");
+        }
+    }
+    st = ra::launch_f32_to_bf16(o_acc, o, (int64_t)N * B * S * H * d, s, &err);
+    return st == RA_OK ? st : fail(st, err ? err : "conversion launch failed");
+}
+
+ra_status ra_check_status(void *workspace, void *stream) {
+    if (!workspace) return fail(RA_ERR_INVALID_ARG, "null workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail(RA_ERR_CUDA, "cudaStreamSynchronize failed");
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return fail(RA_ERR_CUDA, "reading the status word failed");
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return fail(RA_ERR_CUDA, "clearing the status word failed");
+        if (word & ra::RA_DEV_TIMEOUT_BIT)
+            return fail(RA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (status word set)");
+    }
+    return RA_OK;
+}
+
+}  // extern "C"

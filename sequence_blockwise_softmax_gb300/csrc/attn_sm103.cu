@@ -1,0 +1,544 @@
+// attn_sm103.cu -- blockwise exact attention on the sm_103a tensor cores.
+//
+// One CTA owns a "unit": 256 query rows (two 128-row Q tiles) of one
+// (query rank, batch, head).  It sweeps the key/value shards in ring order
+// ("From Ring Attention to DeepSpeed Ulysses to USP", jsqmd.com/news/734632,
+// §3.1: at step s rank i holds the KV of rank (i - s) mod N) and folds every
+// 128-key tile into the running (m, l, O) state of §3.2, so the partial
+// results never leave the SM.
+//
+// Causal masking by position (same article §3.4; "What problem does sequence
+// parallelism solve?", model.playoffer.cn, engineering notes: the ring decides
+// the mask from the token positions).  In every layout a rank's local tokens
+// are in increasing global order, so the keys of shard j that query row a may
+// see are exactly a prefix 0..kc(a)-1 of that shard.  A unit visits only the
+// key tiles that prefix covers for its last row (fully masked tiles are
+// skipped), and each softmax thread masks the columns past its own row's
+// prefix (diagonal tiles are masked in-tile).
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into a
+//               two-stage ring of shared-memory buffers.
+//   warp 1      MMA issuer (one elected lane): S_g = Q_g K^T into tensor
+//               memory, then O_g += P_g V with P_g read from tensor memory.
+//   warp 2      tensor-memory allocator.
+//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
+//               query row (the 32x32b tensor-memory load gives a thread its
+//               whole row, so row max and row sum need no shuffles), exp2
+//               with the scale folded into log2(e), P written back to
+//               tensor memory as bf16, O rescaled in place when the row max
+//               grows, and the final normalisation and store.
+// Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+d), O_1 [256+d, 256+2d); P_g is packed bf16 in the first 64
+// columns of S_g.
+#include <cmath>
+#include <cstdio>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+
+struct AttnArgs {
+    void *o;
+    float *lse;
+    unsigned *status;
+    int B, S, H, N;
+    int layout, causal;
+    float scale_log2;   // softmax scale * log2(e)
+    int num_q_ranks;    // N in ring mode, 1 in block mode
+    int q_rank_fixed;   // block mode: the query rank; ring mode: -1
+    int kv_rank_fixed;  // block mode: the key/value rank; ring mode: -1
+    int num_steps;      // N for a full sweep, 1 for one ring step or block mode
+    int step_base;      // ring mode: the first step visited (0 for a full sweep)
+    int n_units_seq;    // ceil(S / 256)
+};
+
+// Global position of local token s on rank r (the layout formulas of the
+// article's §3.1 contiguous split, §4 striped split and §6.1 zigzag split).
+__device__ __forceinline__ int64_t token_pos(int layout, int r, int64_t s, int N, int64_t S) {
+    if (layout == RA_CONTIGUOUS) return (int64_t)r * S + s;
+    if (layout == RA_STRIPED) return s * N + r;
+    const int64_t C = S >> 1;
+    return s < C ? (int64_t)r * C + s : (int64_t)(2 * N - 1 - r) * C + (s - C);
+}
+
+__device__ __forceinline__ int64_t clamp64(int64_t x, int64_t lo, int64_t hi) {
+    return x < lo ? lo : (x > hi ? hi : x);
+}
+
+// How many keys of rank j sit at global positions <= p.  Because positions
+// increase along a rank's local order, these are local keys 0..result-1.
+__device__ __forceinline__ int64_t keys_upto(int layout, int j, int64_t p, int N, int64_t S) {
+    if (layout == RA_CONTIGUOUS) return clamp64(p - (int64_t)j * S + 1, 0, S);
+    if (layout == RA_STRIPED) return p < j ? 0 : (((p - j) / N + 1) < S ? (p - j) / N + 1 : S);
+    const int64_t C = S >> 1;
+    return clamp64(p - (int64_t)j * C + 1, 0, C) + clamp64(p - (int64_t)(2 * N - 1 - j) * C + 1, 0, C);
+}
+
+// The sequence of (kv rank, key tile) pairs a unit visits.  Every role walks
+// it identically.
+struct TileWalk {
+    int step, tile, ntiles, j;
+    int num_steps, step_base, q_rank, kv_fixed, N, layout, causal, S;
+    int64_t last_pos;
+
+    __device__ void start_step() {
+        while (step < num_steps) {
+            j = kv_fixed >= 0 ? kv_fixed : ((q_rank - step - step_base) % N + N) % N;
+            const int64_t kc = causal ? keys_upto(layout, j, last_pos, N, S) : (int64_t)S;
+            ntiles = (int)((kc + 127) / 128);
+            tile = 0;
+            if (ntiles > 0) return;
+            ++step;
+        }
+    }
+    __device__ bool valid() const { return step < num_steps; }
+    __device__ void next() {
+        if (++tile >= ntiles) {
+            ++step;
+            start_step();
+        }
+    }
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void record_timeout(unsigned *status, volatile int *abort) {
+    *abort = 1;
+    atomicOr(status, RA_DEV_TIMEOUT_BIT);
+}
+
+template <int D>
+struct AttnSmem {
+    static constexpr int kStages = 2;
+    static constexpr uint32_t kTile = 128u * D * 2u;     // 128 rows x d bf16
+    static constexpr uint32_t kBox = 128u * 128u;        // 128 rows x 64 columns
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = 2 * kTile;
+    static constexpr uint32_t kV = kK + kStages * kTile;
+    static constexpr uint32_t kBars = kV + kStages * kTile;
+    // barriers: Q full, K full[2], V full[2], KV empty[2], S full[2], P full[2],
+    // PV done[2], final
+    static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 1;
+    static constexpr uint32_t kMisc = kBars + kNumBars * 8;
+    static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
+};
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const AttnArgs args) {
+    using L = AttnSmem<D>;
+    constexpr int NS = L::kStages;
+    constexpr int HALVES = D / 64;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + L::kBars;
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KVEMPTY = 1 + 2 * NS,
+              B_SFULL = 1 + 3 * NS, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2,
+              B_FINAL = B_PVDONE + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- unit decode: heavy units first (causal work grows with position)
+    const int S = args.S, H = args.H, N = args.N;
+    const int per_bh = args.num_q_ranks * args.n_units_seq;
+    const int bh = blockIdx.x / per_bh;
+    const int rem = blockIdx.x % per_bh;
+    const int b = bh / H, h = bh % H;
+    int qi, qt;
+    if (args.layout == RA_CONTIGUOUS) {
+        qi = args.num_q_ranks - 1 - rem / args.n_units_seq;
+        qt = args.n_units_seq - 1 - rem % args.n_units_seq;
+    } else {
+        qt = args.n_units_seq - 1 - rem / args.num_q_ranks;
+        qi = args.num_q_ranks - 1 - rem % args.num_q_ranks;
+    }
+    const bool ring = args.q_rank_fixed < 0;
+    const int q_rank = ring ? qi : args.q_rank_fixed;
+    const int zq = (ring ? qi * args.B : 0) + b;
+    const int row0 = qt * 256;
+    const int row_end = min(S, row0 + 256);
+
+    TileWalk walk0;
+    walk0.step = 0;
+    walk0.num_steps = args.num_steps;
+    walk0.step_base = args.step_base;
+    walk0.q_rank = q_rank;
+    walk0.kv_fixed = args.kv_rank_fixed;
+    walk0.N = N;
+    walk0.layout = args.layout;
+    walk0.causal = args.causal;
+    walk0.S = S;
+    walk0.last_pos = token_pos(args.layout, q_rank, row_end - 1, N, S);
+
+    // ---- setup
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_QFULL), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(B_KFULL + s), 1);
+            mbar_init(BAR(B_VFULL + s), 1);
+            mbar_init(BAR(B_KVEMPTY + s), 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(BAR(B_SFULL + g), 1);
+            mbar_init(BAR(B_PFULL + g), 128);
+            mbar_init(BAR(B_PVDONE + g), 1);
+        }
+        mbar_init(BAR(B_FINAL), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        const int xh = h * D;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
+            for (int g = 0; g < 2; ++g)
+                for (int c = 0; c < HALVES; ++c)
+                    tma_load_3d(s_base + L::kQ + g * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL),
+                                xh + 64 * c, row0 + 128 * g, zq);
+        }
+        __syncwarp();
+        TileWalk w = walk0;
+        w.start_step();
+        int t = 0;
+        bool ok = true;
+        for (; w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            if (t >= NS) {
+                ok = warp_wait(BAR(B_KVEMPTY + st), ((t / NS) - 1) & 1, abort_flag);
+                if (!ok) break;
+            }
+            if (lane == 0) {
+                const int zkv = (ring ? w.j * args.B : 0) + b;
+                const int y = w.tile * 128;
+                mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
+                for (int c = 0; c < HALVES; ++c)
+                    tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
+                                xh + 64 * c, y, zkv);
+                mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
+                for (int c = 0; c < HALVES; ++c)
+                    tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
+                                xh + 64 * c, y, zkv);
+            }
+            __syncwarp();
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args.status, abort_flag);
+            // let the copies already issued land before the CTA exits
+            volatile int never = 0;
+            mbar_wait(BAR(B_QFULL), 0, &never);
+            for (int u = (t > NS ? t - NS : 0); u < t; ++u) {
+                mbar_wait(BAR(B_KFULL + u % NS), (u / NS) & 1, &never);
+                mbar_wait(BAR(B_VFULL + u % NS), (u / NS) & 1, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
+        TileWalk w = walk0;
+        w.start_step();
+        int t = 0;
+        for (; ok && w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            const uint32_t ph = (t / NS) & 1;
+            if (!(ok = warp_wait(BAR(B_KFULL + st), ph, abort_flag))) break;
+            const uint32_t kbase = s_base + L::kK + st * L::kTile;
+            for (int g = 0; g < 2 && ok; ++g) {
+                // S_g and P_g share columns: PV_g of the previous tile must be done
+                if (t > 0 && !(ok = warp_wait(BAR(B_PVDONE + g), (t - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t qbase = s_base + L::kQ + g * L::kTile;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+                        mma_ss(tmem + g * 128, sdesc_sw128(qbase + off, 16, 1024),
+                               sdesc_sw128(kbase + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(BAR(B_SFULL + g));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
+            const uint32_t vbase = s_base + L::kV + st * L::kTile;
+            for (int g = 0; g < 2 && ok; ++g) {
+                if (!(ok = warp_wait(BAR(B_PFULL + g), t & 1, abort_flag))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + 256 + g * D, tmem + g * 128 + kk * 8,
+                               sdesc_sw128(vbase + kk * 2048, L::kBox, 1024), IDESC_O,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(BAR(B_PVDONE + g));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(BAR(B_KVEMPTY + st));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) record_timeout(args.status, abort_flag);
+        // every MMA issued above has finished before tensor memory is freed
+        if (lane == 0) tc_commit(BAR(B_FINAL));
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(BAR(B_FINAL), 0, &never);
+    } else if (warp >= 4) {
+        // ================================================= softmax
+        const int g = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;                 // row inside Q tile g (= TMEM lane)
+        const int a = row0 + g * 128 + r;             // local query row in the shard
+        const int a_c = a < S ? a : S - 1;
+        const int64_t my_pos = token_pos(args.layout, q_rank, a_c, N, S);
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + g * 128;
+        const uint32_t tO = tmem + lane_off + 256 + g * D;
+        const float sl2 = args.scale_log2;
+
+        float m_ref = -INFINITY;  // running max, already scaled to log2 units
+        float l = 0.f;            // running denominator, relative to m_ref
+        TileWalk w = walk0;
+        w.start_step();
+        int t = 0;
+        bool ok = true;
+        int cur_j = -1;
+        int kc = S;
+        for (; w.valid(); w.next(), ++t) {
+            if (w.j != cur_j || w.tile == 0) {
+                cur_j = w.j;
+                kc = args.causal ? (int)keys_upto(args.layout, w.j, my_pos, N, S) : S;
+            }
+            if (!(ok = warp_wait(BAR(B_SFULL + g), t & 1, abort_flag))) break;
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+            tmem_wait_ld();
+            float *s = reinterpret_cast<float *>(&sr[0][0]);
+            const int lim = kc - w.tile * 128;        // valid key columns for this row
+            if (lim < 128) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float m_new = fmaxf(m_ref, mx * sl2);
+            const bool grow = m_new > m_ref;
+            const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
+            if (grow) {
+                l *= alpha;
+                m_ref = m_new;
+            }
+            // O holds PV of every earlier tile (S_g of this tile was computed
+            // after it); rescale it when any row of the warp grew its max
+            if (t > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + q * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st32(tO + q * 32, o);
+                }
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t pr[2][32];
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+                const float p0 = ex2(fmaf(s[c], sl2, -m_use));
+                const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
+                l += p0 + p1;
+                pr[c >> 6][(c & 63) >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS, pr[0]);
+            tmem_st32(tS + 32, pr[1]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_PFULL + g));
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args.status, abort_flag);
+        } else {
+            const int T = t;
+            if (T > 0) {
+                ok = warp_wait(BAR(B_PVDONE + g), (T - 1) & 1, abort_flag);
+                if (!ok && lane == 0) record_timeout(args.status, abort_flag);
+                tc_fence_after();
+            }
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const bool store = ok && a < S;
+            const size_t orow = ((size_t)zq * S + a) * H + h;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                if (T > 0 && ok) {
+                    tmem_ld32(tO + q * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = 0u;
+                }
+                if (store) {
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.o) + orow * D + q * 32);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
+                                                 __uint_as_float(o[4 * c + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * c + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * c + 3]) * inv_l);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(args.o) + orow * D + q * 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 v4;
+                            v4.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+                            v4.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+                            v4.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+                            v4.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+                            dst[c] = v4;
+                        }
+                    }
+                }
+            }
+            if (store)
+                args.lse[((size_t)zq * H + h) * S + a] =
+                    l > 0.f ? (m_ref + lg2(l)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+
+    // ---- teardown: every role is here, all tensor-core work has finished
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [Z, S, H*d] bf16 viewed as a 3-D tensor, 64-column x 128-row boxes with
+// the 128-byte swizzle the MMA descriptors expect.
+static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)(H * d), (cuuint64_t)S, (cuuint64_t)Z};
+    cuuint64_t strides[2] = {(cuuint64_t)(H * d * 2), (cuuint64_t)(S * H * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool F32>
+static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq, int64_t Zkv,
+                          int64_t grid, cudaStream_t stream, const char **err) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, Zq, a.S, a.H, D) || !make_map(&mk, a.k, Zkv, a.S, a.H, D) ||
+        !make_map(&mv, a.v, Zkv, a.S, a.H, D)) {
+        *err = "cuTensorMapEncodeTiled failed for the q/k/v tensor maps";
+        return RA_ERR_CUDA;
+    }
+    auto kern = attn_fwd_kernel<D, F32>;
+    const int smem = (int)AttnSmem<D>::kBytes;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        *err = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+        return RA_ERR_CUDA;
+    }
+    kern<<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, args);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = cudaGetErrorString(e);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
+ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err) {
+    AttnArgs args;
+    args.o = a.o;
+    args.lse = a.lse;
+    args.status = a.status;
+    args.B = (int)a.B;
+    args.S = (int)a.S;
+    args.H = (int)a.H;
+    args.N = a.N;
+    args.layout = a.layout;
+    args.causal = a.causal ? 1 : 0;
+    const float scale = a.scale > 0.f ? a.scale : 1.0f / std::sqrt((float)a.d);
+    args.scale_log2 = scale * 1.4426950408889634f;
+    args.num_q_ranks = a.ring ? a.N : 1;
+    args.q_rank_fixed = a.ring ? -1 : a.q_rank;
+    args.kv_rank_fixed = a.ring ? -1 : a.kv_rank;
+    args.num_steps = (a.ring && a.ring_step < 0) ? a.N : 1;
+    args.step_base = a.ring_step < 0 ? 0 : a.ring_step;
+    args.n_units_seq = (int)((a.S + 255) / 256);
+    const int64_t Zq = a.ring ? a.N * a.B : a.B;
+    const int64_t Zkv = Zq;
+    const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;
+    if (grid == 0) return RA_OK;
+    if (grid > 0x7fffffffLL) {
+        *err = "too many query tiles for one launch";
+        return RA_ERR_UNSUPPORTED;
+    }
+    if (a.d == 128)
+        return a.out_f32 ? launch_t<128, true>(a, args, Zq, Zkv, grid, stream, err)
+                         : launch_t<128, false>(a, args, Zq, Zkv, grid, stream, err);
+    return a.out_f32 ? launch_t<64, true>(a, args, Zq, Zkv, grid, stream, err)
+                     : launch_t<64, false>(a, args, Zq, Zkv, grid, stream, err);
+}
+
+}  // namespace ra

@@ -1,0 +1,49 @@
+// ra_internal.h -- launchers shared between the C-ABI layer and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+// Bits of the device status word (first 4 bytes of every workspace).
+constexpr unsigned RA_DEV_TIMEOUT_BIT = 1u;
+
+// One attention launch: every query unit of `num_q_ranks` ranks sweeps its
+// key/value shards.  Ring mode: q/k/v are [N, B, S, H, d] stacks, each query
+// rank i visits ranks (i - s) mod N for s = 0..N-1.  Block mode: q is the
+// [B, S, H, d] shard of q_rank, k/v that of kv_rank, one step.
+struct AttnLaunch {
+    const void *q, *k, *v;
+    void *o;            // bf16 (ring) or fp32 (block)
+    float *lse;
+    unsigned *status;   // device status word
+    int64_t B, S, H;
+    int d, N, layout, causal;
+    float scale;
+    bool ring;
+    int q_rank, kv_rank;  // block mode only
+    int ring_step;        // ring mode: -1 sweeps all N steps; s >= 0 runs step s only
+    bool out_f32;
+};
+
+ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);
+
+ra_status launch_permute(const void *src, void *dst, int op, int layout, int64_t B, int64_t L,
+                         int64_t H, int64_t d, int R, int U, int elem_bytes, cudaStream_t stream,
+                         const char **err);
+
+ra_status launch_lse_to_seq(const float *src, float *dst, int layout, int64_t B, int64_t L,
+                            int64_t H, int R, int U, cudaStream_t stream, const char **err);
+
+ra_status launch_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
+                           int64_t B, int64_t S, int64_t H, int d, cudaStream_t stream,
+                           const char **err);
+
+// fp32 -> bf16 copy of n elements (n a multiple of 4): the stepwise ring finish
+ra_status launch_f32_to_bf16(const float *src, void *dst, int64_t n, cudaStream_t stream,
+                             const char **err);
+
+}  // namespace ra

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "ra.h")
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^RA_API\s+[\w\s\*]*?\b(ra_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_four_calls():
+    syms = declared_symbols()
+    for name in ("ra_shard_permute", "ra_block_attn_fwd", "ra_lse_merge", "ra_ring_attn_fwd"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(ralib):
+    lib = ctypes.CDLL(ralib.library_path())
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(ralib.SIGNATURES)
+
+
+def test_version(ralib):
+    assert "sm_103a" in ralib.ra_version()
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails its checks first
+
+
+def _ring(ralib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, L=1024, H=2, d=128, N=4, layout=0,
+             causal=1, scale=0.0, flags=0, ws=FAKE, wsb=256, stream=None)
+    a.update(kw)
+    return ralib.lib().ra_ring_attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"],
+                                        a["H"], a["d"], a["N"], a["layout"], a["causal"], a["scale"],
+                                        a["flags"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(L=1022), 2),                         # N does not divide L
+    (dict(layout=2, L=1028), 2),               # zigzag needs 2N | L
+    (dict(d=96), 3),                           # unsupported head dim
+    (dict(N=0), 2),
+    (dict(layout=7), 1),
+    (dict(flags=8), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(q=0), 1),                            # null pointer
+    (dict(o=FAKE + 8), 4),                     # misaligned
+    (dict(wsb=16), 1),                         # workspace too small
+    (dict(flags=1, wsb=256), 1),               # stepwise needs the big workspace
+])
+def test_ring_rejects_bad_arguments(ralib, kw, status):
+    assert _ring(ralib, **kw) == status
+    assert ralib.lib().ra_last_error().decode()
+
+
+def test_empty_inputs_are_no_ops(ralib):
+    assert _ring(ralib, B=0, q=0, k=0, v=0, o=0, lse=0, ws=0) == 0
+    assert _ring(ralib, L=0, q=0, k=0, v=0, o=0, lse=0, ws=0) == 0
+    lib = ralib.lib()
+    assert lib.ra_shard_permute(None, None, 0, 0, 0, 16, 2, 64, 4, 1, 2, None) == 0
+    assert lib.ra_lse_merge(None, None, None, None, 1, 0, 2, 64, None) == 0
+
+
+def test_permute_rejects_bad_arguments(ralib):
+    lib = ralib.lib()
+    P = lambda *a: lib.ra_shard_permute(FAKE, FAKE + 4096, *a, None)
+    assert P(9, 0, 1, 16, 2, 64, 4, 1, 2) == 1          # op
+    assert P(0, 5, 1, 16, 2, 64, 4, 1, 2) == 1          # layout
+    assert P(0, 0, 1, 18, 2, 64, 4, 1, 2) == 2          # 4 does not divide 18
+    assert P(0, 2, 1, 25, 2, 64, 5, 1, 2) == 2          # zigzag needs 2R | L
+    assert P(2, 0, 1, 16, 3, 64, 2, 2, 2) == 2          # U does not divide H
+    assert P(0, 0, 1, 16, 1, 3, 4, 1, 2) == 4           # 6-byte tokens
+    assert P(0, 0, 1, 16, 2, 64, 4, 1, 3) == 1          # elem_bytes
+    assert lib.ra_shard_permute(FAKE + 2, FAKE, 0, 0, 1, 16, 2, 64, 4, 1, 2, None) == 4
+
+
+def test_block_rejects_bad_ranks(ralib):
+    lib = ralib.lib()
+    st = lib.ra_block_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 4, 0, 0, 1, 0.0,
+                               FAKE, 256, None)
+    assert st == 1
+
+
+def test_workspace_sizes(ralib):
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 0) == 256
+    n = 1 * 1024 * 2 * 128
+    want = 256 + 2 * n * 4 + 1024 * 2 * 4
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 1) == want
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 96, 4, 0) == 0
