@@ -22,7 +22,6 @@ Under torchrun (N > 1) every rank runs its own replica of the workload.
 import argparse
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -147,8 +146,10 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- the GPU path
 class Workload:
-    def __init__(self, ra, name, layout, dev):
-        w = WORKLOADS[name]
+    def __init__(self, ra, name, layout, dev, shape=None):
+        w = dict(WORKLOADS[name])
+        if shape is not None:
+            w.update(B=shape[0], L=shape[1], H=shape[2], d=shape[3], N=shape[4])
         self.ra, self.name, self.layout, self.dev = ra, name, layout, dev
         self.B, self.L, self.H, self.d, self.N = w["B"], w["L"], w["H"], w["d"], w["N"]
         self.U = w.get("U", 1)
@@ -164,12 +165,13 @@ class Workload:
                          for _ in range(3)]
         self.Bq, self.Hq = U * B, H // U
         ring_in = self.head if U > 1 else self.shard
-        self.o_ring = torch.empty_like(ring_in[0])
+        self.o_ring = torch.empty(ring_in[0].shape, dtype=torch.float32, device=dev)
         self.lse_ring = torch.empty((N, self.Bq, self.Hq, L // N), dtype=torch.float32, device=dev)
-        self.o_shard = torch.empty_like(self.shard[0]) if U > 1 else None
-        self.o_seq = torch.empty((B, L, H, d), dtype=torch.bfloat16, device=dev)
+        self.o_shard = (torch.empty(self.shard[0].shape, dtype=torch.float32, device=dev)
+                        if U > 1 else None)
+        self.o_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=dev)
         self.lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
-        self.o_host = torch.empty((B, L, H, d), dtype=torch.bfloat16).pin_memory()
+        self.o_host = torch.empty((B, L, H, d), dtype=torch.float32).pin_memory()
         self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
         self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N), device=dev)
         self.flops = algorithmic_flops(B, L, H, d, self.causal)
@@ -210,7 +212,7 @@ class Workload:
         return sum(t.numel() * t.element_size() for t in self.host)
 
     def d2h_bytes(self):
-        return self.o_host.numel() * 2 + self.lse_host.numel() * 4
+        return self.o_host.numel() * 4 + self.lse_host.numel() * 4
 
 
 def barrier(world):
@@ -224,6 +226,11 @@ def max_over_ranks(x, world, dev):
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(flops_per_rank, world, ms_per_step_max):
+    """Whole-job TFLOP/s: every rank's replica counts, timed by the slowest rank."""
+    return flops_per_rank * world / (ms_per_step_max * 1e-3) / 1e12
 
 
 def timed(fn, steps, world, dev):
@@ -312,6 +319,8 @@ def main():
     ap.add_argument("--layout", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--shape", default=None,
+                    help="B,L,H,d,N override of the workload's sizes (a smaller case for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -331,7 +340,8 @@ def main():
 
     w = WORKLOADS[args.workload]
     layout = args.layout or w["layouts"][0]
-    wl = Workload(ra, args.workload, layout, dev)
+    shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
+    wl = Workload(ra, args.workload, layout, dev, shape)
 
     for _ in range(args.warmup):
         wl.step()
@@ -353,9 +363,8 @@ def main():
     ms_e2e = timed(wl.step_e2e, args.steps, world, dev) / args.steps
     ra.ra_check_status(wl.ws)
 
-    total_flops = wl.flops * world
-    value = total_flops / (ms_step * 1e-3) / 1e12
-    e2e_value = total_flops / (ms_e2e * 1e-3) / 1e12
+    value = job_value(wl.flops, world, ms_step)
+    e2e_value = job_value(wl.flops, world, ms_e2e)
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -366,13 +375,13 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
+        "config": {"workload": args.workload + ("" if shape is None else " (resized)"), "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
                    "d": wl.d, "N": wl.N, "U": wl.U, "causal": wl.causal,
                    "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<128,false> (ra_ring_attn_fwd)",
+                     "kernel": "attn_fwd_kernel<128, fp32 O> (ra_ring_attn_fwd)",
                      "kernel_ms": attn_ms,
                      "peak_source": "%s bf16_tflops_sustained" % peak_src},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),

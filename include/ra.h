@@ -76,6 +76,8 @@ typedef enum {
 
 /* ra_ring_attn_fwd flags */
 #define RA_FLAG_STEPWISE 1u  /* run the sweep as N x (block attention + LSE merge) */
+#define RA_FLAG_O_BF16 2u    /* write O as bf16 (rounded once, to nearest even)
+                                instead of the default fp32 accumulator         */
 
 /* Smallest workspace any attention call accepts (the status word and padding). */
 #define RA_WORKSPACE_MIN_BYTES 256u
@@ -148,10 +150,12 @@ RA_API ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, co
  * i and step s = 0..N-1, query shard i meets key/value shard (i - s) mod N
  * and the results are merged online ([USP] §3.2).  All N ranks run at once.
  * q, k, v: bf16 [N, B, S, H, d] shard stacks (S = L / N) in `layout`;
- * o: bf16 [N, B, S, H, d]; lse: fp32 [N, B, H, S] (natural log).
+ * o: [N, B, S, H, d], fp32 by default (the fp32 accumulator itself), bf16
+ * with RA_FLAG_O_BF16; lse: fp32 [N, B, H, S] (natural log).
  * Requires N | L, 2N | L for zigzag, d in {64, 128}.  scale <= 0 selects
- * 1/sqrt(d).  flags: 0 (fused sweep) or RA_FLAG_STEPWISE.  workspace: device,
- * ra_ring_attn_workspace_bytes() bytes, zero-filled before its first use.
+ * 1/sqrt(d).  flags: any of RA_FLAG_STEPWISE, RA_FLAG_O_BF16.  workspace:
+ * device, ra_ring_attn_workspace_bytes() bytes, zero-filled before its first
+ * use.
  */
 RA_API ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                            int64_t B, int64_t L, int64_t H, int d, int N, int layout,

@@ -21,6 +21,7 @@ RA_OK, RA_ERR_INVALID_ARG, RA_ERR_SHAPE, RA_ERR_UNSUPPORTED, RA_ERR_ALIGNMENT, R
 RA_CONTIGUOUS, RA_STRIPED, RA_ZIGZAG = range(3)
 RA_SEQ_TO_SHARDS, RA_SHARDS_TO_SEQ, RA_ULYSSES_SEQ_TO_HEAD, RA_ULYSSES_HEAD_TO_SEQ = range(4)
 RA_FLAG_STEPWISE = 1
+RA_FLAG_O_BF16 = 2
 RA_WORKSPACE_MIN_BYTES = 256
 LAYOUTS = {"contiguous": RA_CONTIGUOUS, "striped": RA_STRIPED, "zigzag": RA_ZIGZAG}
 
@@ -132,9 +133,12 @@ def ra_ring_attn_workspace_bytes(B, L, H, d, N, flags=0):
 
 def ra_ring_attn_fwd(q, k, v, o, lse, B, L, H, d, N, layout, causal, scale=0.0, flags=0,
                      workspace=None, stream=None):
-    for t in (q, k, v, o):
+    """O may be fp32 (default) or bf16; a bf16 ``o`` sets RA_FLAG_O_BF16."""
+    for t in (q, k, v):
         assert t.dtype == torch.bfloat16
-    assert lse.dtype == torch.float32
+    assert o.dtype in (torch.float32, torch.bfloat16) and lse.dtype == torch.float32
+    if o.dtype == torch.bfloat16:
+        flags |= RA_FLAG_O_BF16
     _check(lib().ra_ring_attn_fwd(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(o, "o"),
                                   _ptr(lse, "lse"), B, L, H, d, N, _layout(layout),
                                   int(bool(causal)), float(scale), int(flags),

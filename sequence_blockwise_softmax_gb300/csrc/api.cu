@@ -24,8 +24,8 @@ bool valid_layout(int layout) {
 }
 
 // Workspace layout: [0, 256) status word + reserved; then, for the stepwise
-// sweep, the fp32 output accumulator and one fp32 partial (O and LSE), each
-// starting on a 256-byte boundary.
+// sweep, the fp32 output accumulator (bf16 O only) and one fp32 partial (O
+// and LSE), each starting on a 256-byte boundary.
 constexpr size_t kHeader = RA_WORKSPACE_MIN_BYTES;
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -34,13 +34,13 @@ struct StepwiseLayout {
     size_t o_acc, o_part, lse_part, total;
 };
 
-StepwiseLayout stepwise_layout(int64_t B, int64_t L, int64_t H, int d, int N) {
+// With an fp32 O the caller's O is the accumulator and needs no workspace copy.
+StepwiseLayout stepwise_layout(int64_t B, int64_t L, int64_t H, int d, bool o_bf16) {
     const size_t n_o = (size_t)B * (size_t)L * (size_t)H * (size_t)d;  // N*B*S*H*d
     const size_t n_lse = (size_t)B * (size_t)L * (size_t)H;
-    (void)N;
     StepwiseLayout s;
     s.o_acc = kHeader;
-    s.o_part = s.o_acc + round256(n_o * 4);
+    s.o_part = s.o_acc + (o_bf16 ? round256(n_o * 4) : 0);
     s.lse_part = s.o_part + round256(n_o * 4);
     s.total = s.lse_part + round256(n_lse * 4);
     return s;
@@ -173,7 +173,8 @@ ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const flo
 
 size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N, unsigned flags) {
     if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
-    if (flags & RA_FLAG_STEPWISE) return stepwise_layout(B, L, H, d, N).total;
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16)) return 0;
+    if (flags & RA_FLAG_STEPWISE) return stepwise_layout(B, L, H, d, (flags & RA_FLAG_O_BF16) != 0).total;
     return kHeader;
 }
 
@@ -181,7 +182,8 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
                            int64_t B, int64_t L, int64_t H, int d, int N, int layout, int causal,
                            float scale, unsigned flags, void *workspace, size_t workspace_bytes,
                            void *stream) {
-    if (flags & ~RA_FLAG_STEPWISE) return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
+    const bool o_bf16 = (flags & RA_FLAG_O_BF16) != 0;
     if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
     if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
     if (L % N) return fail(RA_ERR_SHAPE, "N must divide L");
@@ -217,15 +219,15 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
     if (!(flags & RA_FLAG_STEPWISE)) {
         a.o = o;
         a.ring_step = -1;
-        a.out_f32 = false;
+        a.out_f32 = !o_bf16;
         st = ra::launch_attention(a, s, &err);
         return st == RA_OK ? st : fail(st, err ? err : "attention launch failed");
     }
     // Stepwise: the pages' per-step structure -- at step s every rank meets
     // KV shard (i - s) mod N, then the partial result is merged in.
-    StepwiseLayout wl = stepwise_layout(B, L, H, d, N);
+    StepwiseLayout wl = stepwise_layout(B, L, H, d, o_bf16);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *o_acc = reinterpret_cast<float *>(ws + wl.o_acc);
+    float *o_acc = o_bf16 ? reinterpret_cast<float *>(ws + wl.o_acc) : static_cast<float *>(o);
     float *o_part = reinterpret_cast<float *>(ws + wl.o_part);
     float *lse_part = reinterpret_cast<float *>(ws + wl.lse_part);
     a.out_f32 = true;
@@ -240,6 +242,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
             if (st != RA_OK) return fail(st, err ? err : "merge launch failed");
         }
     }
+    if (!o_bf16) return RA_OK;
     st = ra::launch_f32_to_bf16(o_acc, o, (int64_t)N * B * S * H * d, s, &err);
     return st == RA_OK ? st : fail(st, err ? err : "conversion launch failed");
 }

@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/ra.h"
+#include "ra.h"
 
 namespace ra {
 

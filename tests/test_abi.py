@@ -94,6 +94,9 @@ def test_block_rejects_bad_ranks(ralib):
 def test_workspace_sizes(ralib):
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 0) == 256
     n = 1 * 1024 * 2 * 128
-    want = 256 + 2 * n * 4 + 1024 * 2 * 4
-    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 1) == want
+    # stepwise, fp32 O: one fp32 partial (O and LSE); the caller's O accumulates
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 1) == 256 + n * 4 + 1024 * 2 * 4
+    # stepwise, bf16 O: an fp32 accumulator as well
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 3) == 256 + 2 * n * 4 + 1024 * 2 * 4
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 4) == 0
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 96, 4, 0) == 0

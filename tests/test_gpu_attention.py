@@ -15,7 +15,7 @@ from synthetic_inputs import make_qkv
 pytestmark = pytest.mark.gpu
 
 
-def run_ring(ra, q, k, v, N, layout, causal, flags=0, U=1, scale=0.0):
+def run_ring(ra, q, k, v, N, layout, causal, flags=0, U=1, scale=0.0, o_dtype=torch.float32):
     """Full path on the GPU: shard (and Ulysses) permutes, ring sweep, and back."""
     dev = torch.device("cuda:0")
     B, L, H, d = q.shape
@@ -31,16 +31,17 @@ def run_ring(ra, q, k, v, N, layout, causal, flags=0, U=1, scale=0.0):
             y = z
         seq_sh.append(y)
     Bq, Hq = U * B, H // U
-    o = torch.empty_like(seq_sh[0])
+    o = torch.empty(seq_sh[0].shape, dtype=o_dtype, device=dev)
     lse = torch.empty((R, Bq, Hq, L // R), dtype=torch.float32, device=dev)
-    ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(Bq, L, Hq, d, R, flags))
+    wflags = flags | (ra.RA_FLAG_O_BF16 if o_dtype == torch.bfloat16 else 0)
+    ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(Bq, L, Hq, d, R, wflags))
     ra.ra_ring_attn_fwd(*seq_sh, o, lse, Bq, L, Hq, d, R, layout, causal, scale=scale,
                         flags=flags, workspace=ws)
     if U > 1:
-        o2 = torch.empty((P, B, L // P, H, d), dtype=torch.bfloat16, device=dev)
+        o2 = torch.empty((P, B, L // P, H, d), dtype=o_dtype, device=dev)
         ra.ra_shard_permute(o, o2, ra.RA_ULYSSES_HEAD_TO_SEQ, layout, B, L, H, d, R, U)
         o = o2
-    o_seq = torch.empty((B, L, H, d), dtype=torch.bfloat16, device=dev)
+    o_seq = torch.empty((B, L, H, d), dtype=o_dtype, device=dev)
     ra.ra_shard_permute(o, o_seq, ra.RA_SHARDS_TO_SEQ, layout, B, L, H, d, R, U)
     lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
     ra.ra_lse_to_seq(lse, lse_seq, layout, B, L, H, R, U)
@@ -70,6 +71,21 @@ def test_ring_matches_oracle(ralib, gpu, B, L, H, d, N, layout, causal, flags):
     o, lse = run_ring(ralib, q, k, v, N, layout, causal, flags=flags)
     o_ref, lse_ref = oracle.full_attention(q, k, v, causal=causal)
     assert_attention_close(o, o_ref, lse, lse_ref, "%s N=%d causal=%s" % (layout, N, causal))
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["fused", "stepwise"])
+def test_ring_bf16_output(ralib, gpu, flags):
+    """With RA_FLAG_O_BF16 the output is the fp32 result rounded once to bf16, so it lies
+    within the fp32 bar plus half a bf16 ulp of |O| (2^-8 relative) of the exact result."""
+    q, k, v, _ = make_qkv(1, 1024, 2, 128, seed=31)
+    o, lse = run_ring(ralib, q, k, v, 4, "zigzag", True, flags=flags, o_dtype=torch.bfloat16)
+    o_ref, lse_ref = oracle.full_attention(q, k, v, causal=True)
+    half_ulp = np.abs(o_ref) * 2.0 ** -8
+    assert np.all(np.abs(o - o_ref) <= 1e-2 + half_ulp)
+    assert np.abs(lse - lse_ref).max() <= 1e-3
+    # and it is exactly the fp32 path rounded to bf16
+    o32, _ = run_ring(ralib, q, k, v, 4, "zigzag", True, flags=flags)
+    np.testing.assert_array_equal(o, torch.from_numpy(o32).to(torch.bfloat16).float().numpy())
 
 
 def test_ring_explicit_scale(ralib, gpu):

@@ -37,24 +37,24 @@ def gpu_path(ra, q, k, v, N, layout, causal, U=1, rows=None):
             y = z
         sh.append(y)
     Bq, Hq = U * B, H // U
-    o = torch.empty_like(sh[0])
+    o = torch.empty(sh[0].shape, dtype=torch.float32, device=dev)
     lse = torch.empty((R, Bq, Hq, L // R), dtype=torch.float32, device=dev)
     ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(Bq, L, Hq, d, R))
     ra.ra_ring_attn_fwd(*sh, o, lse, Bq, L, Hq, d, R, layout, causal, workspace=ws)
     del sh
     if U > 1:
-        o2 = torch.empty((P, B, L // P, H, d), dtype=torch.bfloat16, device=dev)
+        o2 = torch.empty((P, B, L // P, H, d), dtype=torch.float32, device=dev)
         ra.ra_shard_permute(o, o2, ra.RA_ULYSSES_HEAD_TO_SEQ, layout, B, L, H, d, R, U)
         o = o2
-    o_seq = torch.empty((B, L, H, d), dtype=torch.bfloat16, device=dev)
+    o_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=dev)
     ra.ra_shard_permute(o, o_seq, ra.RA_SHARDS_TO_SEQ, layout, B, L, H, d, R, U)
     lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
     ra.ra_lse_to_seq(lse, lse_seq, layout, B, L, H, R, U)
     ra.ra_check_status(ws)
     if rows is not None:
         idx = torch.as_tensor(rows, device=dev)
-        return o_seq[:, idx].float().cpu().numpy(), lse_seq[:, :, idx].cpu().numpy()
-    return o_seq.float().cpu().numpy(), lse_seq.cpu().numpy()
+        return o_seq[:, idx].cpu().numpy(), lse_seq[:, :, idx].cpu().numpy()
+    return o_seq.cpu().numpy(), lse_seq.cpu().numpy()
 
 
 def sample_rows(w, layout, scaled_rows, n_random=40, seed=0):
