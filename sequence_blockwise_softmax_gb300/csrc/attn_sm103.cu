@@ -127,6 +127,10 @@ struct AttnSmem {
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
 };
 
+// The softmax reference point of a row moves only when the row max exceeds it
+// by more than this (log2 units), bounding P by 2^8.
+constexpr float kRescaleLog2 = 8.0f;
+
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -214,8 +218,12 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // 384 threads x 168 registers at launch: the producer / MMA / allocator
+    // warpgroup (warps 0-3) gives registers to the two softmax warpgroups,
+    // 128 x 64 + 256 x 216 <= 384 x 168; each role makes the call on entry.
     if (warp == 0) {
         // ================================================= TMA producer
+        regs_shrink<64>();
         const int xh = h * D;
         if (lane == 0) {
             mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
@@ -261,50 +269,78 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer
+        regs_shrink<64>();
+        // Issue order per key tile t (pipe order):
+        //   PV_0(t), S_0(t+1), PV_1(t), S_1(t+1)
+        // so the softmax of tile g for t+1 overlaps PV_{1-g}(t) and
+        // S_{1-g}(t+1).  S_g(t+1) overwrites the columns PV_g(t) reads P_g
+        // from, so it waits for PV_g(t) to finish.
+        auto issue_s = [&](int g, uint32_t kbase) {
+            const uint32_t qbase = s_base + L::kQ + g * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+                mma_ss(tmem + g * 128, sdesc_sw128(qbase + off, 16, 1024),
+                       sdesc_sw128(kbase + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(BAR(B_SFULL + g));
+        };
+        auto issue_pv = [&](int g, uint32_t vbase, bool first) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tmem + 256 + g * D, tmem + g * 128 + kk * 8,
+                       sdesc_sw128(vbase + kk * 2048, L::kBox, 1024), IDESC_O,
+                       (!first || kk > 0) ? 1u : 0u);
+            tc_commit(BAR(B_PVDONE + g));
+        };
         bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
         TileWalk w = walk0;
         w.start_step();
         int t = 0;
-        for (; ok && w.valid(); w.next(), ++t) {
+        if (ok && w.valid()) {
+            ok = warp_wait(BAR(B_KFULL + 0), 0, abort_flag);
+            tc_fence_after();
+            if (ok && lane == 0) {
+                issue_s(0, s_base + L::kK);
+                issue_s(1, s_base + L::kK);
+            }
+            __syncwarp();
+        }
+        while (ok && w.valid()) {
             const int st = t % NS;
             const uint32_t ph = (t / NS) & 1;
-            if (!(ok = warp_wait(BAR(B_KFULL + st), ph, abort_flag))) break;
-            const uint32_t kbase = s_base + L::kK + st * L::kTile;
-            for (int g = 0; g < 2 && ok; ++g) {
-                // S_g and P_g share columns: PV_g of the previous tile must be done
-                if (t > 0 && !(ok = warp_wait(BAR(B_PVDONE + g), (t - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t qbase = s_base + L::kQ + g * L::kTile;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-                        mma_ss(tmem + g * 128, sdesc_sw128(qbase + off, 16, 1024),
-                               sdesc_sw128(kbase + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(BAR(B_SFULL + g));
-                }
-                __syncwarp();
-            }
-            if (!ok) break;
-            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
+            const int st1 = (t + 1) % NS;
+            const uint32_t ph1 = ((t + 1) / NS) & 1;
             const uint32_t vbase = s_base + L::kV + st * L::kTile;
-            for (int g = 0; g < 2 && ok; ++g) {
-                if (!(ok = warp_wait(BAR(B_PFULL + g), t & 1, abort_flag))) break;
+            const uint32_t kbase1 = s_base + L::kK + st1 * L::kTile;
+            w.next();
+            const bool has_next = w.valid();
+            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
+            tc_fence_after();
+            if (lane == 0) issue_pv(0, vbase, t == 0);
+            __syncwarp();
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_KFULL + st1), ph1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_PVDONE + 0), t & 1, abort_flag))) break;
                 tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + 256 + g * D, tmem + g * 128 + kk * 8,
-                               sdesc_sw128(vbase + kk * 2048, L::kBox, 1024), IDESC_O,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(BAR(B_PVDONE + g));
-                }
+                if (lane == 0) issue_s(0, kbase1);
                 __syncwarp();
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(BAR(B_KVEMPTY + st));
+            if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
+            tc_fence_after();
+            if (lane == 0) {
+                issue_pv(1, vbase, t == 0);
+                tc_commit(BAR(B_KVEMPTY + st));
+            }
             __syncwarp();
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_PVDONE + 1), t & 1, abort_flag))) break;
+                tc_fence_after();
+                if (lane == 0) issue_s(1, kbase1);
+                __syncwarp();
+            }
+            ++t;
         }
         if (!ok && lane == 0) record_timeout(args.status, abort_flag);
         // every MMA issued above has finished before tensor memory is freed
@@ -312,8 +348,11 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         volatile int never = 0;
         mbar_wait(BAR(B_FINAL), 0, &never);
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        regs_shrink<64>();
+    } else {
         // ================================================= softmax
+        regs_grow<216>();
         const int g = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;                 // row inside Q tile g (= TMEM lane)
@@ -351,19 +390,29 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx = s[0];
+            // row max: four independent three-input chains
+            float mA = s[0], mB = s[1], mC = s[2], mD = s[3];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool grow = m_new > m_ref;
-            const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-            if (grow) {
+            for (int c = 4; c < 128; c += 8) {
+                mA = max3(mA, s[c], s[c + 1]);
+                mB = max3(mB, s[c + 2], s[c + 3]);
+                mC = max3(mC, s[c + 4], s[c + 5]);
+                mD = max3(mD, s[c + 6], s[c + 7]);
+            }
+            const float m_tile = max3(mA, mB, fmaxf(mC, mD)) * sl2;
+            // Lazy rescale: the reference point moves only when the row max
+            // grows by more than 2^kRescaleLog2, so P stays below 2^8 and O and
+            // l are rescaled rarely.  O / l is the same for any reference point.
+            const bool move = m_tile > m_ref + kRescaleLog2;
+            float alpha = 1.f;
+            if (move) {
+                alpha = ex2(m_ref - m_tile);
                 l *= alpha;
-                m_ref = m_new;
+                m_ref = m_tile;
             }
             // O holds PV of every earlier tile (S_g of this tile was computed
-            // after it); rescale it when any row of the warp grew its max
-            if (t > 0 && __any_sync(0xffffffffu, grow)) {
+            // after it); rescale it when any row of the warp moved its reference
+            if (t > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
@@ -374,17 +423,32 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_st32(tO + q * 32, o);
                 }
             }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t pr[2][32];
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+            // P of each 32-column chunk goes to tensor memory as 16 packed
+            // columns at 16*chunk, over S columns this thread has already read
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
-                const float p0 = ex2(fmaf(s[c], sl2, -m_use));
-                const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
-                l += p0 + p1;
-                pr[c >> 6][(c & 63) >> 1] = pack_bf16x2(p0, p1);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pr[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float x0, x1;
+                    f32x2_split(fma_f32x2(f32x2(s[32 * q + c], s[32 * q + c + 1]), sl2x2, negm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    lsum[(c >> 1) & 3] = add_f32x2(lsum[(c >> 1) & 3], f32x2(p0, p1));
+                    pr[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + 16 * q, pr);
             }
-            tmem_st32(tS, pr[0]);
-            tmem_st32(tS + 32, pr[1]);
+            {
+                float a0, a1, b0, b1, c0, c1, d0, d1;
+                f32x2_split(lsum[0], a0, a1);
+                f32x2_split(lsum[1], b0, b1);
+                f32x2_split(lsum[2], c0, c1);
+                f32x2_split(lsum[3], d0, d1);
+                l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(B_PFULL + g));
