@@ -167,6 +167,31 @@ RA_API size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int 
                                     unsigned flags);
 
 /*
+ * ra_ring_attn_fwd_stepwise_noalloc -- the RA_FLAG_STEPWISE sweep of
+ * ra_ring_attn_fwd (fp32 O), for callers that cannot allocate device memory.
+ * The pages have no counterpart: it exists for code that may not call
+ * cudaMalloc or pass a workspace -- code running inside another framework's
+ * memory pool or allocator callback, plugins handed only their inputs and
+ * outputs, paths where cudaMalloc / cudaFree would synchronise the device.
+ * Its scratch (one fp32 partial O and LSE plus a status word) is a fixed
+ * 64 MiB array owned by the library, held on every GPU that loads this code
+ * until the process exits; a problem needing more than
+ * B*L*H*(d+1)*4 + 256 <= 64 MiB bytes is rejected with RA_ERR_UNSUPPORTED.
+ * Arguments and layouts are those of ra_ring_attn_fwd with flags =
+ * RA_FLAG_STEPWISE; o is fp32.  It allocates nothing.  The first call on
+ * each device looks up the array's device address (which loads this part of
+ * the library on that device); make that first call before any stream
+ * capture.  Every call on a device uses the same array: calls that may
+ * overlap on the GPU (other streams, other threads) race on it and must be
+ * serialised by the caller.  The status word is cleared at the start of each
+ * call; a wait that runs out is not reported back by this entry point.
+ */
+RA_API ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void *k, const void *v,
+                                                   float *o, float *lse, int64_t B, int64_t L,
+                                                   int64_t H, int d, int N, int layout,
+                                                   int causal, float scale, void *stream);
+
+/*
  * ra_check_status -- synchronise `stream`, read the status word at the start
  * of `workspace`, clear it, and return RA_ERR_TIMEOUT if a kernel recorded a
  * timeout since the last check (RA_OK otherwise).

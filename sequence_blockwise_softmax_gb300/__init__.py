@@ -37,6 +37,8 @@ SIGNATURES = {
     "ra_ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _F, _U, _P,
                               _SZ, _P]),
     "ra_ring_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I, _U]),
+    "ra_ring_attn_fwd_stepwise_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I,
+                                               _F, _P]),
     "ra_check_status": (_I, [_P, _P]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),
@@ -144,6 +146,18 @@ def ra_ring_attn_fwd(q, k, v, o, lse, B, L, H, d, N, layout, causal, scale=0.0, 
                                   int(bool(causal)), float(scale), int(flags),
                                   _ptr(workspace, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ra_ring_attn_fwd_stepwise_noalloc(q, k, v, o, lse, B, L, H, d, N, layout, causal, scale=0.0,
+                                      stream=None):
+    """Stepwise sweep with the library's own fixed scratch array; O is fp32."""
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16
+    assert o.dtype == torch.float32 and lse.dtype == torch.float32
+    _check(lib().ra_ring_attn_fwd_stepwise_noalloc(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"),
+                                                   _ptr(o, "o"), _ptr(lse, "lse"), B, L, H, d, N,
+                                                   _layout(layout), int(bool(causal)), float(scale),
+                                                   _stream(stream)))
 
 
 def ra_check_status(workspace, stream=None):

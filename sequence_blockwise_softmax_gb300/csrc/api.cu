@@ -65,6 +65,8 @@ ra_status check_attn_common(int64_t B, int64_t S, int64_t H, int d, int N, int l
 
 }  // namespace
 
+ra_status ra::set_error(ra_status st, const char *msg) { return fail(st, msg); }
+
 extern "C" {
 
 const char *ra_last_error(void) { return g_last_error.c_str(); }

@@ -46,4 +46,7 @@ ra_status launch_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const
 ra_status launch_f32_to_bf16(const float *src, void *dst, int64_t n, cudaStream_t stream,
                              const char **err);
 
+// Record `msg` as this host thread's ra_last_error() text and return `st`.
+ra_status set_error(ra_status st, const char *msg);
+
 }  // namespace ra
