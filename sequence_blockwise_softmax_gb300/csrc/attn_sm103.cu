@@ -120,16 +120,17 @@ struct AttnSmem {
     static constexpr uint32_t kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBars = kV + kStages * kTile;
-    // barriers: Q full, K full[2], V full[2], KV empty[2], S full[2], P full[2],
-    // PV done[2], final
-    static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 1;
+    // barriers: Q full, K full[2], V full[2], K empty[2], V empty[2], S full[2],
+    // P full[2], PV done[2], final
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
 };
 
-// The softmax reference point of a row moves only when the row max exceeds it
-// by more than this (log2 units), bounding P by 2^8.
-constexpr float kRescaleLog2 = 8.0f;
+// The softmax reference point of a row moves when the row max exceeds it by
+// more than this (log2 units).  Zero keeps the reference at the running max,
+// so the largest P of a row is exactly 1 and carries no bf16 rounding.
+constexpr float kRescaleLog2 = 0.0f;
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(384, 1)
@@ -146,9 +147,9 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KVEMPTY = 1 + 2 * NS,
-              B_SFULL = 1 + 3 * NS, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2,
-              B_FINAL = B_PVDONE + 2;
+    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KEMPTY = 1 + 2 * NS,
+              B_VEMPTY = 1 + 3 * NS, B_SFULL = 1 + 4 * NS, B_PFULL = B_SFULL + 2,
+              B_PVDONE = B_PFULL + 2, B_FINAL = B_PVDONE + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
 
@@ -193,7 +194,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(B_KFULL + s), 1);
             mbar_init(BAR(B_VFULL + s), 1);
-            mbar_init(BAR(B_KVEMPTY + s), 1);
+            mbar_init(BAR(B_KEMPTY + s), 1);
+            mbar_init(BAR(B_VEMPTY + s), 1);
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(BAR(B_SFULL + g), 1);
@@ -235,37 +237,42 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         TileWalk w = walk0;
         w.start_step();
-        int t = 0;
+        int t = 0, k_issued = 0, v_issued = 0;
         bool ok = true;
         for (; w.valid(); w.next(), ++t) {
+            // K of a stage is free once both S MMAs of its tile are done, V
+            // once both PV MMAs are; K therefore refills about a tile earlier
             const int st = t % NS;
-            if (t >= NS) {
-                ok = warp_wait(BAR(B_KVEMPTY + st), ((t / NS) - 1) & 1, abort_flag);
-                if (!ok) break;
-            }
+            const int zkv = (ring ? w.j * args.B : 0) + b;
+            const int y = w.tile * 128;
+            if (t >= NS && !(ok = warp_wait(BAR(B_KEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
-                const int zkv = (ring ? w.j * args.B : 0) + b;
-                const int y = w.tile * 128;
                 mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
                     tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
                                 xh + 64 * c, y, zkv);
+            }
+            __syncwarp();
+            k_issued = t + 1;
+            if (t >= NS && !(ok = warp_wait(BAR(B_VEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
                     tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
                                 xh + 64 * c, y, zkv);
             }
             __syncwarp();
+            v_issued = t + 1;
         }
         if (!ok) {
             if (lane == 0) record_timeout(args.status, abort_flag);
             // let the copies already issued land before the CTA exits
             volatile int never = 0;
             mbar_wait(BAR(B_QFULL), 0, &never);
-            for (int u = (t > NS ? t - NS : 0); u < t; ++u) {
+            for (int u = (k_issued > NS ? k_issued - NS : 0); u < k_issued; ++u)
                 mbar_wait(BAR(B_KFULL + u % NS), (u / NS) & 1, &never);
+            for (int u = (v_issued > NS ? v_issued - NS : 0); u < v_issued; ++u)
                 mbar_wait(BAR(B_VFULL + u % NS), (u / NS) & 1, &never);
-            }
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer
@@ -303,6 +310,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok && lane == 0) {
                 issue_s(0, s_base + L::kK);
                 issue_s(1, s_base + L::kK);
+                tc_commit(BAR(B_KEMPTY + 0));
             }
             __syncwarp();
         }
@@ -331,13 +339,16 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             if (lane == 0) {
                 issue_pv(1, vbase, t == 0);
-                tc_commit(BAR(B_KVEMPTY + st));
+                tc_commit(BAR(B_VEMPTY + st));
             }
             __syncwarp();
             if (has_next) {
                 if (!(ok = warp_wait(BAR(B_PVDONE + 1), t & 1, abort_flag))) break;
                 tc_fence_after();
-                if (lane == 0) issue_s(1, kbase1);
+                if (lane == 0) {
+                    issue_s(1, kbase1);
+                    tc_commit(BAR(B_KEMPTY + st1));
+                }
                 __syncwarp();
             }
             ++t;
@@ -366,6 +377,7 @@ __global__ void __launch_bounds__(384, 1)
 
         float m_ref = -INFINITY;  // running max, already scaled to log2 units
         float l = 0.f;            // running denominator, relative to m_ref
+        float lr = 0.f;           // the same sum over the bf16-rounded P the MMA uses
         TileWalk w = walk0;
         w.start_step();
         int t = 0;
@@ -408,6 +420,7 @@ __global__ void __launch_bounds__(384, 1)
             if (move) {
                 alpha = ex2(m_ref - m_tile);
                 l *= alpha;
+                lr *= alpha;
                 m_ref = m_tile;
             }
             // O holds PV of every earlier tile (S_g of this tile was computed
@@ -426,6 +439,7 @@ __global__ void __launch_bounds__(384, 1)
             const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
             const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
             uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
             // P of each 32-column chunk goes to tensor memory as 16 packed
             // columns at 16*chunk, over S columns this thread has already read
 #pragma unroll
@@ -437,7 +451,9 @@ __global__ void __launch_bounds__(384, 1)
                     f32x2_split(fma_f32x2(f32x2(s[32 * q + c], s[32 * q + c + 1]), sl2x2, negm2), x0, x1);
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     lsum[(c >> 1) & 3] = add_f32x2(lsum[(c >> 1) & 3], f32x2(p0, p1));
-                    pr[c >> 1] = pack_bf16x2(p0, p1);
+                    const uint32_t pk = pack_bf16x2(p0, p1);
+                    pr[c >> 1] = pk;
+                    rs[(c >> 1) & 3] = add_bf16x2_to_f32(rs[(c >> 1) & 3], pk);
                 }
                 tmem_st16(tS + 16 * q, pr);
             }
@@ -448,6 +464,7 @@ __global__ void __launch_bounds__(384, 1)
                 f32x2_split(lsum[2], c0, c1);
                 f32x2_split(lsum[3], d0, d1);
                 l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                lr += (rs[0] + rs[1]) + (rs[2] + rs[3]);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -462,7 +479,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (!ok && lane == 0) record_timeout(args.status, abort_flag);
                 tc_fence_after();
             }
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
             const bool store = ok && a < S;
             const size_t orow = ((size_t)zq * S + a) * H + h;
 #pragma unroll

@@ -244,6 +244,15 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// acc + lo + hi of a packed bf16x2, each half added to the fp32 accumulator
+// exactly as the mixed-precision add rounds it (round to nearest)
+__device__ __forceinline__ float add_bf16x2_to_f32(float acc, uint32_t pk) {
+    unsigned short lo, hi;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(pk));
+    asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(acc) : "h"(lo), "f"(acc));
+    asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(acc) : "h"(hi), "f"(acc));
+    return acc;
+}
 // three-input maximum
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
