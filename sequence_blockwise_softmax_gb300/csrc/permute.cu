@@ -3,10 +3,9 @@
 //
 // A token's [H, d] (or its [H/U, d] head slice) is one contiguous run of
 // bytes ("slab") in both source and destination, so every op is a gather
-// or scatter of slabs.  Each thread moves one 16-byte vector; consecutive
-// threads walk a slab, then the next slab, so loads and stores are
-// 16-byte-vectorised and coalesced.  The grid is a multiple of the SM count
-// and loops over the work.
+// or scatter of slabs.  A warp moves one slab at a time with 16-byte loads
+// and stores (coalesced: consecutive lanes take consecutive vectors).  The
+// grid is a multiple of the SM count and loops over the slabs.
 //
 // Index formulas ("From Ring Attention to DeepSpeed Ulysses to USP",
 // jsqmd.com/news/734632): §4 contiguous / striped split, §6.1 zigzag split,
@@ -56,43 +55,62 @@ struct PermArgs {
     int64_t seq_slab_vecs;    // vectors per full-token [H, d] run (Ulysses ops)
 };
 
+// Byte offsets (in 16-byte vectors) of one slab copy: its place in the shard
+// / head-sharded stack and its place on the other side.
+__device__ __forceinline__ void slab_ends(const PermArgs &a, int64_t slab, int64_t &shard_vec,
+                                          int64_t &other_vec) {
+    if (a.op == RA_SEQ_TO_SHARDS || a.op == RA_SHARDS_TO_SEQ) {
+        // slab indexes the shard stack [P, B, Lp]
+        const int64_t s = slab % a.Lp;
+        const int64_t rest = slab / a.Lp;
+        const int64_t b = rest % a.B;
+        const int64_t p = rest / a.B;
+        const int64_t u = p / a.R, r = p - u * a.R;
+        const int64_t t = layout_pos(a.layout, r, u * a.Lp + s, a.R, a.L / a.R);
+        shard_vec = slab * a.slab_vecs;
+        other_vec = (b * a.L + t) * a.slab_vecs;
+    } else {
+        // slab indexes the head-sharded state [R, U(head group), B, U(member), Lp]
+        int64_t rest = slab;
+        const int64_t s = rest % a.Lp;
+        rest /= a.Lp;
+        const int64_t u = rest % a.U;
+        rest /= a.U;
+        const int64_t b = rest % a.B;
+        rest /= a.B;
+        const int64_t up = rest % a.U;
+        const int64_t r = rest / a.U;
+        const int64_t tok = ((u * a.R + r) * a.B + b) * a.Lp + s;   // seq-sharded token slab
+        shard_vec = slab * a.slab_vecs;
+        other_vec = tok * a.seq_slab_vecs + up * a.slab_vecs;
+    }
+}
+
+// One warp per slab: the index arithmetic runs once per slab, then the lanes
+// stream the slab with 16-byte loads, up to four in flight per lane.
 __global__ void __launch_bounds__(256) permute_kernel(const PermArgs a) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t n_slabs = a.total_vecs / a.slab_vecs;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.src);
     uint4 *dst = reinterpret_cast<uint4 *>(a.dst);
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < a.total_vecs; v += stride) {
-        const int64_t slab = v / a.slab_vecs;
-        const int64_t within = v - slab * a.slab_vecs;
-        int64_t shard_vec, other_vec;  // the two ends of this copy, in vectors
-        if (a.op == RA_SEQ_TO_SHARDS || a.op == RA_SHARDS_TO_SEQ) {
-            // slab indexes the shard stack [P, B, Lp]
-            int64_t s = slab % a.Lp;
-            int64_t rest = slab / a.Lp;
-            const int64_t b = rest % a.B;
-            const int64_t p = rest / a.B;
-            const int64_t u = p / a.R, r = p - u * a.R;
-            const int64_t t = layout_pos(a.layout, r, u * a.Lp + s, a.R, a.L / a.R);
-            shard_vec = slab * a.slab_vecs + within;
-            other_vec = (b * a.L + t) * a.slab_vecs + within;
-            if (a.op == RA_SEQ_TO_SHARDS) dst[shard_vec] = src[other_vec];
-            else dst[other_vec] = src[shard_vec];
-        } else {
-            // slab indexes the head-sharded state [R, U(head group), B, U(member), Lp]
-            int64_t rest = slab;
-            const int64_t s = rest % a.Lp;
-            rest /= a.Lp;
-            const int64_t u = rest % a.U;
-            rest /= a.U;
-            const int64_t b = rest % a.B;
-            rest /= a.B;
-            const int64_t up = rest % a.U;
-            const int64_t r = rest / a.U;
-            const int64_t tok = ((u * a.R + r) * a.B + b) * a.Lp + s;   // seq-sharded token slab
-            shard_vec = slab * a.slab_vecs + within;
-            other_vec = tok * a.seq_slab_vecs + up * a.slab_vecs + within;
-            if (a.op == RA_ULYSSES_SEQ_TO_HEAD) dst[shard_vec] = src[other_vec];
-            else dst[other_vec] = src[shard_vec];
+    const bool gather = a.op == RA_SEQ_TO_SHARDS || a.op == RA_ULYSSES_SEQ_TO_HEAD;
+    for (int64_t slab = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); slab < n_slabs;
+         slab += warps) {
+        int64_t shard_vec, other_vec;
+        slab_ends(a, slab, shard_vec, other_vec);
+        const uint4 *from = src + (gather ? other_vec : shard_vec);
+        uint4 *to = dst + (gather ? shard_vec : other_vec);
+        const int n = (int)a.slab_vecs;
+        int i = lane;
+        for (; i + 96 < n; i += 128) {
+            const uint4 x0 = from[i], x1 = from[i + 32], x2 = from[i + 64], x3 = from[i + 96];
+            to[i] = x0;
+            to[i + 32] = x1;
+            to[i + 64] = x2;
+            to[i + 96] = x3;
         }
+        for (; i < n; i += 32) to[i] = from[i];
     }
 }
 
@@ -159,7 +177,8 @@ ra_status launch_permute(const void *src, void *dst, int op, int layout, int64_t
         a.total_vecs = B * L * a.seq_slab_vecs;
     }
     if (a.total_vecs == 0) return RA_OK;
-    permute_kernel<<<grid_for(a.total_vecs, 256, 8), 256, 0, stream>>>(a);
+    const int64_t n_slabs = a.total_vecs / a.slab_vecs;
+    permute_kernel<<<grid_for(n_slabs * 32, 256, 8), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *err = cudaGetErrorString(e);
