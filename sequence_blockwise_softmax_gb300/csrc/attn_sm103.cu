@@ -282,23 +282,43 @@ __global__ void __launch_bounds__(384, 1)
         // so the softmax of tile g for t+1 overlaps PV_{1-g}(t) and
         // S_{1-g}(t+1).  S_g(t+1) overwrites the columns PV_g(t) reads P_g
         // from, so it waits for PV_g(t) to finish.
-        auto issue_s = [&](int g, uint32_t kbase) {
-            const uint32_t qbase = s_base + L::kQ + g * L::kTile;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-                mma_ss(tmem + g * 128, sdesc_sw128(qbase + off, 16, 1024),
-                       sdesc_sw128(kbase + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        // Descriptors are built once; each k-step adds a compile-time offset
+        // (16-byte units) to the start-address field: 32 B per 16-element step
+        // inside a 64-column box, one box (16 KB) for columns 64-127 of Q and
+        // K, and 16 rows (2 KB) per step of V.  The whole warp runs the issue
+        // code and elect.sync picks the issuing lane.
+        const uint64_t dq[2] = {sdesc_sw128(s_base + L::kQ, 16, 1024),
+                                sdesc_sw128(s_base + L::kQ + L::kTile, 16, 1024)};
+        const uint64_t dk0 = sdesc_sw128(s_base + L::kK, 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(s_base + L::kV, L::kBox, 1024);
+        auto issue_s = [&](int g, int stage) {
+            const uint64_t a0 = dq[g], b0 = dk0 + (uint64_t)(stage * (L::kTile >> 4));
+            const uint32_t d = tmem + g * 128;
+            mma_ss_elect<0, 0>(d, a0, b0, IDESC_S, 0u);
+            mma_ss_elect<2, 2>(d, a0, b0, IDESC_S, 1u);
+            mma_ss_elect<4, 4>(d, a0, b0, IDESC_S, 1u);
+            mma_ss_elect<6, 6>(d, a0, b0, IDESC_S, 1u);
+            if (D == 128) {
+                constexpr uint32_t h = L::kBox >> 4;
+                mma_ss_elect<h, h>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 2, h + 2>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 4, h + 4>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 6, h + 6>(d, a0, b0, IDESC_S, 1u);
             }
-            tc_commit(BAR(B_SFULL + g));
+            tc_commit_elect(BAR(B_SFULL + g));
         };
-        auto issue_pv = [&](int g, uint32_t vbase, bool first) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ts(tmem + 256 + g * D, tmem + g * 128 + kk * 8,
-                       sdesc_sw128(vbase + kk * 2048, L::kBox, 1024), IDESC_O,
-                       (!first || kk > 0) ? 1u : 0u);
-            tc_commit(BAR(B_PVDONE + g));
+        auto issue_pv = [&](int g, int stage, bool first) {
+            const uint64_t b0 = dv0 + (uint64_t)(stage * (L::kTile >> 4));
+            const uint32_t d = tmem + 256 + g * D, a = tmem + g * 128;
+            mma_ts_elect<0, 0>(d, a, b0, IDESC_O, first ? 0u : 1u);
+            mma_ts_elect<8, 128>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<16, 256>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<24, 384>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<32, 512>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<40, 640>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<48, 768>(d, a, b0, IDESC_O, 1u);
+            mma_ts_elect<56, 896>(d, a, b0, IDESC_O, 1u);
+            tc_commit_elect(BAR(B_PVDONE + g));
         };
         bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
         TileWalk w = walk0;
@@ -307,10 +327,10 @@ __global__ void __launch_bounds__(384, 1)
         if (ok && w.valid()) {
             ok = warp_wait(BAR(B_KFULL + 0), 0, abort_flag);
             tc_fence_after();
-            if (ok && lane == 0) {
-                issue_s(0, s_base + L::kK);
-                issue_s(1, s_base + L::kK);
-                tc_commit(BAR(B_KEMPTY + 0));
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc_commit_elect(BAR(B_KEMPTY + 0));
             }
             __syncwarp();
         }
@@ -319,43 +339,38 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t ph = (t / NS) & 1;
             const int st1 = (t + 1) % NS;
             const uint32_t ph1 = ((t + 1) / NS) & 1;
-            const uint32_t vbase = s_base + L::kV + st * L::kTile;
-            const uint32_t kbase1 = s_base + L::kK + st1 * L::kTile;
             w.next();
             const bool has_next = w.valid();
             if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
             if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
             tc_fence_after();
-            if (lane == 0) issue_pv(0, vbase, t == 0);
+            issue_pv(0, st, t == 0);
             __syncwarp();
             if (has_next) {
                 if (!(ok = warp_wait(BAR(B_KFULL + st1), ph1, abort_flag))) break;
                 if (!(ok = warp_wait(BAR(B_PVDONE + 0), t & 1, abort_flag))) break;
                 tc_fence_after();
-                if (lane == 0) issue_s(0, kbase1);
+                issue_s(0, st1);
                 __syncwarp();
             }
             if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
             tc_fence_after();
-            if (lane == 0) {
-                issue_pv(1, vbase, t == 0);
-                tc_commit(BAR(B_VEMPTY + st));
-            }
+            issue_pv(1, st, t == 0);
+            tc_commit_elect(BAR(B_VEMPTY + st));
             __syncwarp();
             if (has_next) {
                 if (!(ok = warp_wait(BAR(B_PVDONE + 1), t & 1, abort_flag))) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    issue_s(1, kbase1);
-                    tc_commit(BAR(B_KEMPTY + st1));
-                }
+                issue_s(1, st1);
+                tc_commit_elect(BAR(B_KEMPTY + st1));
                 __syncwarp();
             }
             ++t;
         }
         if (!ok && lane == 0) record_timeout(args.status, abort_flag);
         // every MMA issued above has finished before tensor memory is freed
-        if (lane == 0) tc_commit(BAR(B_FINAL));
+        __syncwarp();
+        tc_commit_elect(BAR(B_FINAL));
         __syncwarp();
         volatile int never = 0;
         mbar_wait(BAR(B_FINAL), 0, &never);
