@@ -146,7 +146,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- the GPU path
 class Workload:
-    def __init__(self, ra, name, layout, dev, shape=None):
+    def __init__(self, ra, name, layout, dev, shape=None, stepwise=False):
         w = dict(WORKLOADS[name])
         if shape is not None:
             w.update(B=shape[0], L=shape[1], H=shape[2], d=shape[3], N=shape[4])
@@ -173,9 +173,12 @@ class Workload:
         self.lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
         self.o_host = torch.empty((B, L, H, d), dtype=torch.float32).pin_memory()
         self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
-        self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N), device=dev)
+        self.flags = ra.RA_FLAG_STEPWISE if stepwise else 0
+        self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N, self.flags),
+                                   device=dev)
         self.flops = algorithmic_flops(B, L, H, d, self.causal)
-        self.launches = 3 * (2 if U > 1 else 1) + 1 + (2 if U > 1 else 1) + 1
+        attn_launches = (2 * N - 1) if stepwise else 1     # N block sweeps + N-1 merges
+        self.launches = 3 * (2 if U > 1 else 1) + attn_launches + (2 if U > 1 else 1) + 1
         self.attn_events = []
 
     def step(self, time_attention=False):
@@ -190,7 +193,7 @@ class Workload:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
         ra.ra_ring_attn_fwd(*ring_in, self.o_ring, self.lse_ring, self.Bq, L, self.Hq, d, N, self.layout,
-                            self.causal, workspace=self.ws)
+                            self.causal, flags=self.flags, workspace=self.ws)
         if time_attention:
             e1.record()
             self.attn_events.append((e0, e1))
@@ -319,6 +322,8 @@ def main():
     ap.add_argument("--layout", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--stepwise", action="store_true",
+                    help="run the sweep as N block launches + N-1 LSE merges (the pages' per-step loop)")
     ap.add_argument("--shape", default=None,
                     help="B,L,H,d,N override of the workload's sizes (a smaller case for profiling)")
     args = ap.parse_args()
@@ -341,7 +346,7 @@ def main():
     w = WORKLOADS[args.workload]
     layout = args.layout or w["layouts"][0]
     shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
-    wl = Workload(ra, args.workload, layout, dev, shape)
+    wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise)
 
     for _ in range(args.warmup):
         wl.step()
@@ -378,10 +383,12 @@ def main():
         "config": {"workload": args.workload + ("" if shape is None else " (resized)"), "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
                    "d": wl.d, "N": wl.N, "U": wl.U, "causal": wl.causal,
                    "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
+                   "sweep": "stepwise" if args.stepwise else "fused",
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<128, fp32 O> (ra_ring_attn_fwd)",
+                     "kernel": ("ra_ring_attn_fwd stepwise: N x attn_fwd_kernel<fp32 partial> + N-1 x lse_merge_kernel"
+                                if args.stepwise else "attn_fwd_kernel<128, fp32 O> (ra_ring_attn_fwd)"),
                      "kernel_ms": attn_ms,
                      "peak_source": "%s bf16_tflops_sustained" % peak_src},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),

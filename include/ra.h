@@ -78,6 +78,12 @@ typedef enum {
 #define RA_FLAG_STEPWISE 1u  /* run the sweep as N x (block attention + LSE merge) */
 #define RA_FLAG_O_BF16 2u    /* write O as bf16 (rounded once, to nearest even)
                                 instead of the default fp32 accumulator         */
+/* Test hook for the timeout path: the first CTA of the fused sweep never
+ * loads one key tile, so the waits that depend on it run out after about two
+ * seconds; the kernel records RA_ERR_TIMEOUT in the status word, releases what
+ * it holds and exits, and the outputs of that CTA are left unwritten.  Nothing
+ * faults and the context stays usable.  Not for production use.              */
+#define RA_FLAG_INJECT_STALL 0x80000000u
 
 /* Smallest workspace any attention call accepts (the status word and padding). */
 #define RA_WORKSPACE_MIN_BYTES 256u
@@ -153,7 +159,8 @@ RA_API ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, co
  * o: [N, B, S, H, d], fp32 by default (the fp32 accumulator itself), bf16
  * with RA_FLAG_O_BF16; lse: fp32 [N, B, H, S] (natural log).
  * Requires N | L, 2N | L for zigzag, d in {64, 128}.  scale <= 0 selects
- * 1/sqrt(d).  flags: any of RA_FLAG_STEPWISE, RA_FLAG_O_BF16.  workspace:
+ * 1/sqrt(d).  flags: any of RA_FLAG_STEPWISE, RA_FLAG_O_BF16 (and the test
+ * hook RA_FLAG_INJECT_STALL, fused sweep only).  workspace:
  * device, ra_ring_attn_workspace_bytes() bytes, zero-filled before its first
  * use.
  */
@@ -161,6 +168,26 @@ RA_API ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, v
                            int64_t B, int64_t L, int64_t H, int d, int N, int layout,
                            int causal, float scale, unsigned flags,
                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Grouped-query attention ([USP] §5.3: K and V carry fewer heads than Q).
+ * The same calls with H_kv key/value heads: k and v are [.., H_kv, d]
+ * instead of [.., H, d], and query head h attends with key/value head
+ * h / (H / H_kv).  H_kv must divide H; H_kv = H is the plain call.  Every
+ * other argument, layout and behaviour is that of ra_block_attn_fwd /
+ * ra_ring_attn_fwd (the workspace size does not depend on H_kv).  For the
+ * Ulysses permutes of K and V pass H_kv as H (U must divide H_kv).
+ */
+RA_API ra_status ra_block_attn_fwd_gqa(const void *q, const void *k, const void *v, float *o,
+                                       float *lse, int64_t B, int64_t S, int64_t H, int64_t H_kv,
+                                       int d, int N, int q_rank, int kv_rank, int layout,
+                                       int causal, float scale, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+RA_API ra_status ra_ring_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int64_t B, int64_t L, int64_t H, int64_t H_kv,
+                                      int d, int N, int layout, int causal, float scale,
+                                      unsigned flags, void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /* Workspace bytes ra_ring_attn_fwd needs for these arguments (0 on bad ones). */
 RA_API size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N,

@@ -54,7 +54,7 @@ def _load():
         I64 = ctypes.c_int64
         lib.oracle_attention_fp64.argtypes = [
             P, I64, P, I64, P, P, I64, P, I64,
-            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, P, P, ctypes.c_int]
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, P, P, ctypes.c_int]
         lib.oracle_attention_fp64.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -76,7 +76,10 @@ def _bf16_bits(x):
 
 
 def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthreads=0):
-    """fp64 attention of the query rows ``q`` [nq, H, d] against keys ``k``, ``v`` [nk, H, d].
+    """fp64 attention of the query rows ``q`` [nq, H, d] against keys ``k``, ``v`` [nk, Hkv, d].
+
+    With Hkv < H (grouped-query attention) query head h reads key/value head
+    h // (H // Hkv).
 
     Inputs are bf16 (torch bf16 tensors or uint16 bit arrays).  ``q_pos`` /
     ``k_pos`` are the rows' global token positions (default 0..n-1); with
@@ -85,8 +88,8 @@ def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthread
     """
     qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
     nq, H, d = qb.shape
-    nk = kb.shape[0]
-    assert kb.shape == (nk, H, d) and vb.shape == (nk, H, d)
+    nk, Hkv = kb.shape[0], kb.shape[1]
+    assert kb.shape == (nk, Hkv, d) and vb.shape == (nk, Hkv, d) and H % Hkv == 0
     q_pos = np.arange(nq, dtype=np.int64) if q_pos is None else np.ascontiguousarray(q_pos, dtype=np.int64)
     k_pos = np.arange(nk, dtype=np.int64) if k_pos is None else np.ascontiguousarray(k_pos, dtype=np.int64)
     assert q_pos.shape == (nq,) and k_pos.shape == (nk,)
@@ -96,8 +99,10 @@ def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthread
     lse = np.empty((nq, H), dtype=np.float64)
     rc = _load().oracle_attention_fp64(
         qb.ctypes.data, H * d, q_pos.ctypes.data, nq,
-        kb.ctypes.data, vb.ctypes.data, H * d, k_pos.ctypes.data, nk,
-        H, d, float(scale), int(bool(causal)), o.ctypes.data, lse.ctypes.data, int(nthreads))
+        kb.ctypes.data, vb.ctypes.data, Hkv * d, k_pos.ctypes.data, nk,
+        H, Hkv, d, float(scale), int(bool(causal)), o.ctypes.data, lse.ctypes.data, int(nthreads))
+    if rc == -2:
+        raise ValueError("the key/value head count must divide the query head count")
     if rc != 0:
         raise MemoryError("oracle scratch allocation failed")
     return o, lse

@@ -22,6 +22,10 @@
  * A key is allowed when the call is non-causal, or when its global position
  * is not after the query's.  A row with no allowed key gets LSE = -inf, O = 0.
  *
+ * Grouped-query attention (same article, §5.3 on GQA, where K and V have
+ * fewer heads than Q): with Hkv key/value heads, query head h reads key/value
+ * head h / (H / Hkv); Hkv = H is ordinary multi-head attention.
+ *
  * Inputs are bf16 bit patterns; each is widened to float exactly (bf16 is the
  * top half of an IEEE float) and every product and sum is taken in double.
  */
@@ -42,17 +46,19 @@ static inline double bf16_to_double(uint16_t bits) {
 
 /*
  * q:    [nq, H, d] bf16 bits, row iq at q + iq*q_stride (q_stride in elements)
- * k, v: [nk, H, d] bf16 bits, row ik at k + ik*kv_stride
+ * k, v: [nk, Hkv, d] bf16 bits, row ik at k + ik*kv_stride
  * q_pos[nq], k_pos[nk]: global token positions (used only when causal != 0)
  * o:    [nq, H, d] double;  lse: [nq, H] double
- * Returns 0, or -1 when a scratch allocation fails.
+ * Returns 0, -1 when a scratch allocation fails, -2 when Hkv does not divide H.
  */
 int oracle_attention_fp64(const uint16_t *q, int64_t q_stride, const int64_t *q_pos, int64_t nq,
                           const uint16_t *k, const uint16_t *v, int64_t kv_stride,
                           const int64_t *k_pos, int64_t nk,
-                          int H, int d, double scale, int causal,
+                          int H, int Hkv, int d, double scale, int causal,
                           double *o, double *lse, int nthreads) {
     int failed = 0;
+    if (Hkv <= 0 || H % Hkv != 0) return -2;
+    const int group = H / Hkv;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #else
@@ -79,7 +85,7 @@ int oracle_attention_fp64(const uint16_t *q, int64_t q_stride, const int64_t *q_
                 int64_t n_allowed = 0;
                 for (int64_t ik = 0; ik < nk; ++ik) {
                     if (causal && k_pos[ik] > q_pos[iq]) { s[ik] = -INFINITY; continue; }
-                    const uint16_t *kp = k + ik * kv_stride + (int64_t)h * d;
+                    const uint16_t *kp = k + ik * kv_stride + (int64_t)(h / group) * d;
                     double dot = 0.0;
                     for (int e = 0; e < d; ++e) dot += qrow[e] * bf16_to_double(kp[e]);
                     s[ik] = scale * dot;
@@ -99,7 +105,7 @@ int oracle_attention_fp64(const uint16_t *q, int64_t q_stride, const int64_t *q_
                     if (s[ik] == -INFINITY) continue;
                     double p = exp(s[ik] - m);
                     l += p;
-                    const uint16_t *vp = v + ik * kv_stride + (int64_t)h * d;
+                    const uint16_t *vp = v + ik * kv_stride + (int64_t)(h / group) * d;
                     for (int e = 0; e < d; ++e) acc[e] += p * bf16_to_double(vp[e]);
                 }
                 for (int e = 0; e < d; ++e) orow[e] = acc[e] / l;

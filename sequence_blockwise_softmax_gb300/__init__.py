@@ -22,6 +22,7 @@ RA_CONTIGUOUS, RA_STRIPED, RA_ZIGZAG = range(3)
 RA_SEQ_TO_SHARDS, RA_SHARDS_TO_SEQ, RA_ULYSSES_SEQ_TO_HEAD, RA_ULYSSES_HEAD_TO_SEQ = range(4)
 RA_FLAG_STEPWISE = 1
 RA_FLAG_O_BF16 = 2
+RA_FLAG_INJECT_STALL = 0x80000000
 RA_WORKSPACE_MIN_BYTES = 256
 LAYOUTS = {"contiguous": RA_CONTIGUOUS, "striped": RA_STRIPED, "zigzag": RA_ZIGZAG}
 
@@ -37,6 +38,10 @@ SIGNATURES = {
     "ra_ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _F, _U, _P,
                               _SZ, _P]),
     "ra_ring_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I, _U]),
+    "ra_block_attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _I, _I,
+                                   _F, _P, _SZ, _P]),
+    "ra_ring_attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _F, _U,
+                                  _P, _SZ, _P]),
     "ra_ring_attn_fwd_stepwise_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I,
                                                _F, _P]),
     "ra_check_status": (_I, [_P, _P]),
@@ -158,6 +163,34 @@ def ra_ring_attn_fwd_stepwise_noalloc(q, k, v, o, lse, B, L, H, d, N, layout, ca
                                                    _ptr(o, "o"), _ptr(lse, "lse"), B, L, H, d, N,
                                                    _layout(layout), int(bool(causal)), float(scale),
                                                    _stream(stream)))
+
+
+def ra_block_attn_fwd_gqa(q, k, v, o, lse, B, S, H, H_kv, d, N, q_rank, kv_rank, layout, causal,
+                          scale=0.0, workspace=None, stream=None):
+    """ra_block_attn_fwd with H_kv key/value heads (k, v are [B, S, H_kv, d])."""
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16
+    assert o.dtype == torch.float32 and lse.dtype == torch.float32
+    _check(lib().ra_block_attn_fwd_gqa(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(o, "o"),
+                                       _ptr(lse, "lse"), B, S, H, H_kv, d, N, q_rank, kv_rank,
+                                       _layout(layout), int(bool(causal)), float(scale),
+                                       _ptr(workspace, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ra_ring_attn_fwd_gqa(q, k, v, o, lse, B, L, H, H_kv, d, N, layout, causal, scale=0.0, flags=0,
+                         workspace=None, stream=None):
+    """ra_ring_attn_fwd with H_kv key/value heads (k, v are [N, B, S, H_kv, d])."""
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16
+    assert o.dtype in (torch.float32, torch.bfloat16) and lse.dtype == torch.float32
+    if o.dtype == torch.bfloat16:
+        flags |= RA_FLAG_O_BF16
+    _check(lib().ra_ring_attn_fwd_gqa(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(o, "o"),
+                                      _ptr(lse, "lse"), B, L, H, H_kv, d, N, _layout(layout),
+                                      int(bool(causal)), float(scale), int(flags),
+                                      _ptr(workspace, "workspace"),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def ra_check_status(workspace, stream=None):

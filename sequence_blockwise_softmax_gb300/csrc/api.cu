@@ -119,12 +119,23 @@ ra_status ra_lse_to_seq(const float *src, float *dst, int layout, int64_t B, int
     return st == RA_OK ? st : fail(st, err ? err : "lse_to_seq launch failed");
 }
 
-ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *o, float *lse,
-                            int64_t B, int64_t S, int64_t H, int d, int N, int q_rank, int kv_rank,
-                            int layout, int causal, float scale, void *workspace,
-                            size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+ra_status check_kv_heads(int64_t H, int64_t H_kv) {
+    if (H_kv < 1 || H_kv > H || H % H_kv)
+        return fail(RA_ERR_SHAPE, "the key/value head count must divide the query head count");
+    return RA_OK;
+}
+
+ra_status block_attn(const void *q, const void *k, const void *v, float *o, float *lse, int64_t B,
+                     int64_t S, int64_t H, int64_t H_kv, int d, int N, int q_rank, int kv_rank,
+                     int layout, int causal, float scale, void *workspace, size_t workspace_bytes,
+                     void *stream) {
     ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
     if (st != RA_OK) return st;
+    if (H > 0 && (st = check_kv_heads(H, H_kv)) != RA_OK) return st;
     if (q_rank < 0 || q_rank >= N || kv_rank < 0 || kv_rank >= N)
         return fail(RA_ERR_INVALID_ARG, "q_rank and kv_rank must lie in [0, N)");
     if (B * S * H == 0) return RA_OK;
@@ -144,6 +155,7 @@ ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *
     a.B = B;
     a.S = S;
     a.H = H;
+    a.H_kv = H_kv;
     a.d = d;
     a.N = N;
     a.layout = layout;
@@ -157,6 +169,26 @@ ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *
     const char *err = nullptr;
     st = ra::launch_attention(a, static_cast<cudaStream_t>(stream), &err);
     return st == RA_OK ? st : fail(st, err ? err : "attention launch failed");
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, float *o, float *lse,
+                            int64_t B, int64_t S, int64_t H, int d, int N, int q_rank, int kv_rank,
+                            int layout, int causal, float scale, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    return block_attn(q, k, v, o, lse, B, S, H, H, d, N, q_rank, kv_rank, layout, causal, scale,
+                      workspace, workspace_bytes, stream);
+}
+
+ra_status ra_block_attn_fwd_gqa(const void *q, const void *k, const void *v, float *o, float *lse,
+                                int64_t B, int64_t S, int64_t H, int64_t H_kv, int d, int N,
+                                int q_rank, int kv_rank, int layout, int causal, float scale,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    return block_attn(q, k, v, o, lse, B, S, H, H_kv, d, N, q_rank, kv_rank, layout, causal, scale,
+                      workspace, workspace_bytes, stream);
 }
 
 ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b, int64_t B,
@@ -175,16 +207,23 @@ ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const flo
 
 size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N, unsigned flags) {
     if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
-    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16)) return 0;
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_INJECT_STALL)) return 0;
     if (flags & RA_FLAG_STEPWISE) return stepwise_layout(B, L, H, d, (flags & RA_FLAG_O_BF16) != 0).total;
     return kHeader;
 }
 
-ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                           int64_t B, int64_t L, int64_t H, int d, int N, int layout, int causal,
-                           float scale, unsigned flags, void *workspace, size_t workspace_bytes,
-                           void *stream) {
-    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
+}  // extern "C"
+
+namespace {
+
+ra_status ring_attn(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                    int64_t L, int64_t H, int64_t H_kv, int d, int N, int layout, int causal,
+                    float scale, unsigned flags, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_INJECT_STALL))
+        return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
+    if ((flags & RA_FLAG_INJECT_STALL) && (flags & RA_FLAG_STEPWISE))
+        return fail(RA_ERR_INVALID_ARG, "RA_FLAG_INJECT_STALL applies to the fused sweep only");
     const bool o_bf16 = (flags & RA_FLAG_O_BF16) != 0;
     if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
     if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
@@ -193,6 +232,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
     const int64_t S = L / N;
     ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
     if (st != RA_OK) return st;
+    if (H > 0 && (st = check_kv_heads(H, H_kv)) != RA_OK) return st;
     if (B * L * H == 0) return RA_OK;
     if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -212,6 +252,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
     a.B = B;
     a.S = S;
     a.H = H;
+    a.H_kv = H_kv;
     a.d = d;
     a.N = N;
     a.layout = layout;
@@ -222,6 +263,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
         a.o = o;
         a.ring_step = -1;
         a.out_f32 = !o_bf16;
+        a.inject_stall = (flags & RA_FLAG_INJECT_STALL) != 0;
         st = ra::launch_attention(a, s, &err);
         return st == RA_OK ? st : fail(st, err ? err : "attention launch failed");
     }
@@ -247,6 +289,26 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
     if (!o_bf16) return RA_OK;
     st = ra::launch_f32_to_bf16(o_acc, o, (int64_t)N * B * S * H * d, s, &err);
     return st == RA_OK ? st : fail(st, err ? err : "conversion launch failed");
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t L, int64_t H, int d, int N, int layout, int causal,
+                           float scale, unsigned flags, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    return ring_attn(q, k, v, o, lse, B, L, H, H, d, N, layout, causal, scale, flags, workspace,
+                     workspace_bytes, stream);
+}
+
+ra_status ra_ring_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int64_t B, int64_t L, int64_t H, int64_t H_kv, int d, int N,
+                               int layout, int causal, float scale, unsigned flags,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    return ring_attn(q, k, v, o, lse, B, L, H, H_kv, d, N, layout, causal, scale, flags, workspace,
+                     workspace_bytes, stream);
 }
 
 ra_status ra_check_status(void *workspace, void *stream) {

@@ -52,6 +52,8 @@ struct AttnArgs {
     int num_steps;      // N for a full sweep, 1 for one ring step or block mode
     int step_base;      // ring mode: the first step visited (0 for a full sweep)
     int n_units_seq;    // ceil(S / 256)
+    int inject_stall;   // test hook: CTA 0 never loads its second K tile
+    int kv_group;       // query heads per key/value head (1 without GQA)
 };
 
 // Global position of local token s on rank r (the layout formulas of the
@@ -127,10 +129,10 @@ struct AttnSmem {
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
 };
 
-// The softmax reference point of a row moves when the row max exceeds it by
-// more than this (log2 units).  Zero keeps the reference at the running max,
-// so the largest P of a row is exactly 1 and carries no bf16 rounding.
-constexpr float kRescaleLog2 = 0.0f;
+// The softmax reference point of a row moves only when the row max exceeds it
+// by more than this (log2 units), so P stays below 2^8 and O is rescaled
+// rarely; O / l does not depend on the reference point.
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(384, 1)
@@ -226,7 +228,8 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ================================================= TMA producer
         regs_shrink<64>();
-        const int xh = h * D;
+        const int xh = h * D;                        // Q columns of head h
+        const int xkv = (h / args.kv_group) * D;     // K/V columns of its key/value head
         if (lane == 0) {
             mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
             for (int g = 0; g < 2; ++g)
@@ -246,20 +249,21 @@ __global__ void __launch_bounds__(384, 1)
             const int zkv = (ring ? w.j * args.B : 0) + b;
             const int y = w.tile * 128;
             if (t >= NS && !(ok = warp_wait(BAR(B_KEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
-            if (lane == 0) {
+            const bool withhold = args.inject_stall && blockIdx.x == 0 && t == 1;
+            if (lane == 0 && !withhold) {
                 mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
                     tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
-                                xh + 64 * c, y, zkv);
+                                xkv + 64 * c, y, zkv);
             }
             __syncwarp();
-            k_issued = t + 1;
+            if (!withhold) k_issued = t + 1;
             if (t >= NS && !(ok = warp_wait(BAR(B_VEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
                     tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
-                                xh + 64 * c, y, zkv);
+                                xkv + 64 * c, y, zkv);
             }
             __syncwarp();
             v_issued = t + 1;
@@ -583,8 +587,9 @@ template <int D, bool F32>
 static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq, int64_t Zkv,
                           int64_t grid, cudaStream_t stream, const char **err) {
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, Zq, a.S, a.H, D) || !make_map(&mk, a.k, Zkv, a.S, a.H, D) ||
-        !make_map(&mv, a.v, Zkv, a.S, a.H, D)) {
+    const int64_t Hkv = a.H_kv > 0 ? a.H_kv : a.H;
+    if (!make_map(&mq, a.q, Zq, a.S, a.H, D) || !make_map(&mk, a.k, Zkv, a.S, Hkv, D) ||
+        !make_map(&mv, a.v, Zkv, a.S, Hkv, D)) {
         *err = "cuTensorMapEncodeTiled failed for the q/k/v tensor maps";
         return RA_ERR_CUDA;
     }
@@ -622,6 +627,8 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     args.num_steps = (a.ring && a.ring_step < 0) ? a.N : 1;
     args.step_base = a.ring_step < 0 ? 0 : a.ring_step;
     args.n_units_seq = (int)((a.S + 255) / 256);
+    args.inject_stall = a.inject_stall ? 1 : 0;
+    args.kv_group = (int)(a.H / (a.H_kv > 0 ? a.H_kv : a.H));
     const int64_t Zq = a.ring ? a.N * a.B : a.B;
     const int64_t Zkv = Zq;
     const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;

@@ -21,12 +21,14 @@ struct AttnLaunch {
     float *lse;
     unsigned *status;   // device status word
     int64_t B, S, H;
+    int64_t H_kv;         // key/value heads (grouped-query attention); 0 means H
     int d, N, layout, causal;
     float scale;
     bool ring;
     int q_rank, kv_rank;  // block mode only
     int ring_step;        // ring mode: -1 sweeps all N steps; s >= 0 runs step s only
     bool out_f32;
+    bool inject_stall;    // test hook, see RA_FLAG_INJECT_STALL
 };
 
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);

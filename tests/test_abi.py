@@ -52,6 +52,7 @@ def _ring(ralib, **kw):
     (dict(N=0), 2),
     (dict(layout=7), 1),
     (dict(flags=8), 1),
+    (dict(flags=0x80000001), 1),               # the stall hook is fused-sweep only
     (dict(scale=float("nan")), 1),
     (dict(q=0), 1),                            # null pointer
     (dict(o=FAKE + 8), 4),                     # misaligned
@@ -89,6 +90,17 @@ def test_block_rejects_bad_ranks(ralib):
     st = lib.ra_block_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 4, 0, 0, 1, 0.0,
                                FAKE, 256, None)
     assert st == 1
+
+
+def test_gqa_rejects_bad_head_counts_on_host(ralib):
+    lib = ralib.lib()
+    for hkv in (3, 0, 16):
+        st = lib.ra_ring_attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1024, 8, hkv, 128, 4, 0, 1, 0.0, 0,
+                                      FAKE, 256, None)
+        assert st == 2
+    st = lib.ra_block_attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 8, 3, 128, 4, 0, 0, 0, 1, 0.0,
+                                   FAKE, 256, None)
+    assert st == 2
 
 
 def test_workspace_sizes(ralib):

@@ -158,3 +158,39 @@ def test_pins_catch_off_by_one_mask(ora):
     # a mask that also lets row t see key t+1
     o, _ = ora.attention(q, k, v, q_pos=np.arange(L) + 1, causal=True)
     assert np.abs(o[0] - v[0].double().numpy()).max() > 1e-2
+
+
+# --- grouped-query attention ("From Ring Attention to DeepSpeed Ulysses to USP", §5.3) ---
+
+def test_gqa_hand_case(ora):
+    """Two query heads share one key/value head: both rows follow the 2x2 hand case."""
+    q = _bits([[[1.0, 0.0], [1.0, 0.0]], [[0.0, 1.0], [0.0, 1.0]]])     # [L=2, H=2, d=2]
+    k = _bits([[[1.0, 0.0]], [[0.0, 1.0]]])                              # [L=2, Hkv=1, d=2]
+    v = _bits([[[1.0, 2.0]], [[3.0, 4.0]]])
+    rows = {r[0] + r[3]: r for r in read_golden("hand_2x2.txt")}
+    o, lse = ora.attention(q, k, v, scale=1.0)
+    for h in range(2):
+        assert o[0, h, 0] == pytest.approx(float(rows["noncausal0"][4]), abs=1e-14)
+        assert o[1, h, 1] == pytest.approx(float(rows["noncausal1"][5]), abs=1e-14)
+        assert lse[0, h] == pytest.approx(float(rows["noncausal0"][6]), abs=1e-14)
+
+
+def test_gqa_zero_queries_closed_form(ora):
+    """Q = 0 with 4 query heads per key/value head: head h averages v of head h // 4."""
+    L, H, Hkv, d = 21, 8, 2, 16
+    q = torch.zeros((L, H, d), dtype=torch.bfloat16)
+    k = randn_bf16((L, Hkv, d), 41)
+    v = randn_bf16((L, Hkv, d), 42)
+    o, lse = ora.attention(q, k, v, causal=True)
+    vf = v.double().numpy()
+    for t in range(L):
+        for h in range(H):
+            np.testing.assert_allclose(o[t, h], vf[:t + 1, h // 4].mean(axis=0), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[t], np.full(H, math.log(t + 1)), rtol=0, atol=1e-13)
+
+
+def test_gqa_rejects_bad_head_counts(ora):
+    q = randn_bf16((3, 3, 4), 1)
+    k = randn_bf16((3, 2, 4), 2)
+    with pytest.raises((ValueError, AssertionError)):
+        ora.attention(q, k, k)
