@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from synthetic_inputs import WORKLOADS, make_qkv  # noqa: E402
+from synthetic_inputs import WORKLOADS, make_cu_seqlens, make_qkv  # noqa: E402
 
 METRIC = "causal ring-attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
 DEFAULT_WORKLOAD = "striped_B1_H8_L131072_d128_N16"
@@ -146,7 +146,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- the GPU path
 class Workload:
-    def __init__(self, ra, name, layout, dev, shape=None, stepwise=False):
+    def __init__(self, ra, name, layout, dev, shape=None, stepwise=False, kv_heads=None, varlen=None):
         w = dict(WORKLOADS[name])
         if shape is not None:
             w.update(B=shape[0], L=shape[1], H=shape[2], d=shape[3], N=shape[4])
@@ -155,14 +155,20 @@ class Workload:
         self.U = w.get("U", 1)
         self.causal = w["causal"]
         B, L, H, d, N, U = self.B, self.L, self.H, self.d, self.N, self.U
+        self.Hkv = kv_heads or H
         q, k, v, _ = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])
+        if self.Hkv != H:
+            # grouped-query attention: the first H_kv heads of the drawn K and V
+            k, v = k[:, :, :self.Hkv].contiguous(), v[:, :, :self.Hkv].contiguous()
         self.host = [t.pin_memory() for t in (q, k, v)]
         self.seq = [t.to(dev) for t in self.host]
         P = U * N
-        self.shard = [torch.empty((P, B, L // P, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        self.heads = [H, self.Hkv, self.Hkv]
+        self.shard = [torch.empty((P, B, L // P, hx, d), dtype=torch.bfloat16, device=dev)
+                      for hx in self.heads]
         if U > 1:
-            self.head = [torch.empty((N, U, B, L // N, H // U, d), dtype=torch.bfloat16, device=dev)
-                         for _ in range(3)]
+            self.head = [torch.empty((N, U, B, L // N, hx // U, d), dtype=torch.bfloat16, device=dev)
+                         for hx in self.heads]
         self.Bq, self.Hq = U * B, H // U
         ring_in = self.head if U > 1 else self.shard
         self.o_ring = torch.empty(ring_in[0].shape, dtype=torch.float32, device=dev)
@@ -177,6 +183,15 @@ class Workload:
         self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N, self.flags),
                                    device=dev)
         self.flops = algorithmic_flops(B, L, H, d, self.causal)
+        self.cu = None
+        if varlen:
+            if B != 1 or U != 1:
+                raise ValueError("packed sequences need B = 1 and no Ulysses split")
+            cu = make_cu_seqlens(L, varlen, w["seed"])
+            lens = (cu[1:] - cu[:-1]).double()
+            pairs = float((lens * (lens + 1) / 2).sum()) if self.causal else float((lens * lens).sum())
+            self.flops = 4.0 * H * d * pairs
+            self.cu = cu.to(torch.int32).to(dev)
         attn_launches = (2 * N - 1) if stepwise else 1     # N block sweeps + N-1 merges
         self.launches = 3 * (2 if U > 1 else 1) + attn_launches + (2 if U > 1 else 1) + 1
         self.attn_events = []
@@ -184,16 +199,24 @@ class Workload:
     def step(self, time_attention=False):
         ra, B, L, H, d, N, U = self.ra, self.B, self.L, self.H, self.d, self.N, self.U
         for i in range(3):
-            ra.ra_shard_permute(self.seq[i], self.shard[i], ra.RA_SEQ_TO_SHARDS, self.layout, B, L, H, d, N, U)
+            hx = self.heads[i]
+            ra.ra_shard_permute(self.seq[i], self.shard[i], ra.RA_SEQ_TO_SHARDS, self.layout, B, L, hx, d, N, U)
             if U > 1:
                 ra.ra_shard_permute(self.shard[i], self.head[i], ra.RA_ULYSSES_SEQ_TO_HEAD, self.layout,
-                                    B, L, H, d, N, U)
+                                    B, L, hx, d, N, U)
         ring_in = self.head if U > 1 else self.shard
         if time_attention:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-        ra.ra_ring_attn_fwd(*ring_in, self.o_ring, self.lse_ring, self.Bq, L, self.Hq, d, N, self.layout,
-                            self.causal, flags=self.flags, workspace=self.ws)
+        if self.cu is not None:
+            ra.ra_ring_attn_fwd_varlen(*ring_in, self.o_ring, self.lse_ring, self.cu, L, H, self.Hkv, d, N,
+                                       self.layout, self.causal, flags=self.flags, workspace=self.ws)
+        elif self.Hkv == H:
+            ra.ra_ring_attn_fwd(*ring_in, self.o_ring, self.lse_ring, self.Bq, L, self.Hq, d, N, self.layout,
+                                self.causal, flags=self.flags, workspace=self.ws)
+        else:
+            ra.ra_ring_attn_fwd_gqa(*ring_in, self.o_ring, self.lse_ring, self.Bq, L, self.Hq, self.Hkv // U,
+                                    d, N, self.layout, self.causal, flags=self.flags, workspace=self.ws)
         if time_attention:
             e1.record()
             self.attn_events.append((e0, e1))
@@ -324,6 +347,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--stepwise", action="store_true",
                     help="run the sweep as N block launches + N-1 LSE merges (the pages' per-step loop)")
+    ap.add_argument("--varlen", type=int, default=None,
+                    help="pack this many variable-length sequences (seeded cut points) into the workload")
+    ap.add_argument("--kv-heads", type=int, default=None,
+                    help="grouped-query attention with this many key/value heads")
     ap.add_argument("--shape", default=None,
                     help="B,L,H,d,N override of the workload's sizes (a smaller case for profiling)")
     args = ap.parse_args()
@@ -346,7 +373,8 @@ def main():
     w = WORKLOADS[args.workload]
     layout = args.layout or w["layouts"][0]
     shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
-    wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise)
+    wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise, kv_heads=args.kv_heads,
+                  varlen=args.varlen)
 
     for _ in range(args.warmup):
         wl.step()
@@ -381,7 +409,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload + ("" if shape is None else " (resized)"), "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
-                   "d": wl.d, "N": wl.N, "U": wl.U, "causal": wl.causal,
+                   "d": wl.d, "N": wl.N, "U": wl.U, "H_kv": wl.Hkv, "causal": wl.causal,
+                   "packed_sequences": args.varlen,
                    "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
                    "sweep": "stepwise" if args.stepwise else "fused",
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},

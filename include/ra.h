@@ -189,6 +189,23 @@ RA_API ra_status ra_ring_attn_fwd_gqa(const void *q, const void *k, const void *
                                       unsigned flags, void *workspace, size_t workspace_bytes,
                                       void *stream);
 
+/*
+ * ra_ring_attn_fwd_varlen -- the ring sweep over packed variable-length
+ * sequences ([USP] §6.2 runs a varlen kernel per ring step; §8 names variable
+ * lengths as harder for the ring).  The n_seqs sequences are packed into one
+ * stream of L tokens (B = 1): cu_seqlens (device, int32, n_seqs + 1 entries)
+ * holds their boundaries, 0 = c_0 <= c_1 <= ... <= c_n = L (empty sequences
+ * allowed).  The layout shards the packed stream by global position; a query
+ * sees only keys of its own sequence (and, causal, not after it).  Boundaries
+ * that break these rules give wrong masks but never an out-of-range access.
+ * q [N, 1, S, H, d], k and v [N, 1, S, H_kv, d]; the rest as ra_ring_attn_fwd_gqa.
+ */
+RA_API ra_status ra_ring_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                                         float *lse, const int32_t *cu_seqlens, int n_seqs,
+                                         int64_t L, int64_t H, int64_t H_kv, int d, int N,
+                                         int layout, int causal, float scale, unsigned flags,
+                                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Workspace bytes ra_ring_attn_fwd needs for these arguments (0 on bad ones). */
 RA_API size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N,
                                     unsigned flags);

@@ -53,7 +53,7 @@ def _load():
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         lib.oracle_attention_fp64.argtypes = [
-            P, I64, P, I64, P, P, I64, P, I64,
+            P, I64, P, I64, P, P, I64, P, I64, P, P,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, P, P, ctypes.c_int]
         lib.oracle_attention_fp64.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -75,11 +75,19 @@ def _bf16_bits(x):
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthreads=0):
+def segment_ids(cu_seqlens, positions):
+    """Sequence id of each global position for packed sequences with boundaries cu_seqlens."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return np.searchsorted(cu, np.asarray(positions, dtype=np.int64), side="right") - 1
+
+
+def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthreads=0,
+              q_seg=None, k_seg=None):
     """fp64 attention of the query rows ``q`` [nq, H, d] against keys ``k``, ``v`` [nk, Hkv, d].
 
     With Hkv < H (grouped-query attention) query head h reads key/value head
-    h // (H // Hkv).
+    h // (H // Hkv).  With ``q_seg`` / ``k_seg`` (sequence ids of packed
+    sequences) a key is allowed only within the query's own sequence.
 
     Inputs are bf16 (torch bf16 tensors or uint16 bit arrays).  ``q_pos`` /
     ``k_pos`` are the rows' global token positions (default 0..n-1); with
@@ -95,11 +103,18 @@ def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthread
     assert q_pos.shape == (nq,) and k_pos.shape == (nk,)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
+    if (q_seg is None) != (k_seg is None):
+        raise ValueError("give both q_seg and k_seg, or neither")
+    if q_seg is not None:
+        q_seg = np.ascontiguousarray(q_seg, dtype=np.int64)
+        k_seg = np.ascontiguousarray(k_seg, dtype=np.int64)
+        assert q_seg.shape == (nq,) and k_seg.shape == (nk,)
     o = np.empty((nq, H, d), dtype=np.float64)
     lse = np.empty((nq, H), dtype=np.float64)
     rc = _load().oracle_attention_fp64(
         qb.ctypes.data, H * d, q_pos.ctypes.data, nq,
         kb.ctypes.data, vb.ctypes.data, Hkv * d, k_pos.ctypes.data, nk,
+        None if q_seg is None else q_seg.ctypes.data, None if k_seg is None else k_seg.ctypes.data,
         H, Hkv, d, float(scale), int(bool(causal)), o.ctypes.data, lse.ctypes.data, int(nthreads))
     if rc == -2:
         raise ValueError("the key/value head count must divide the query head count")
@@ -108,8 +123,11 @@ def attention(q, k, v, q_pos=None, k_pos=None, causal=False, scale=None, nthread
     return o, lse
 
 
-def full_attention(q, k, v, causal, scale=None, rows=None, nthreads=0):
+def full_attention(q, k, v, causal, scale=None, rows=None, nthreads=0, cu_seqlens=None):
     """Attention over a whole sequence, [B, L, H, d] inputs.
+
+    ``cu_seqlens``: optional boundaries of packed sequences (0 = c_0 <= ... <= c_n = L);
+    a query then attends only within its own sequence.
 
     ``rows``: optional int array of query positions to evaluate (all if None).
     Returns (O [B, nrows, H, d], LSE [B, H, nrows]) in float64.
@@ -117,10 +135,12 @@ def full_attention(q, k, v, causal, scale=None, rows=None, nthreads=0):
     B, L = q.shape[0], q.shape[1]
     idx = np.arange(L, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
     qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    seg_all = None if cu_seqlens is None else segment_ids(cu_seqlens, np.arange(L))
     outs, lses = [], []
     for b in range(B):
         o, lse = attention(qb[b][idx], kb[b], vb[b], q_pos=idx, k_pos=None,
-                           causal=causal, scale=scale, nthreads=nthreads)
+                           causal=causal, scale=scale, nthreads=nthreads,
+                           q_seg=None if seg_all is None else seg_all[idx], k_seg=seg_all)
         outs.append(o)
         lses.append(lse.T)
     return np.stack(outs), np.stack(lses)

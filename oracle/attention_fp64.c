@@ -26,6 +26,11 @@
  * fewer heads than Q): with Hkv key/value heads, query head h reads key/value
  * head h / (H / Hkv); Hkv = H is ordinary multi-head attention.
  *
+ * Packed variable-length sequences (same article, §6 and §8: Megatron's
+ * varlen kernel, and variable-length support as a ring weak spot): when
+ * segment ids are given, a key is allowed only if it belongs to the query's
+ * own sequence (and, causal, is not after it).
+ *
  * Inputs are bf16 bit patterns; each is widened to float exactly (bf16 is the
  * top half of an IEEE float) and every product and sum is taken in double.
  */
@@ -48,12 +53,14 @@ static inline double bf16_to_double(uint16_t bits) {
  * q:    [nq, H, d] bf16 bits, row iq at q + iq*q_stride (q_stride in elements)
  * k, v: [nk, Hkv, d] bf16 bits, row ik at k + ik*kv_stride
  * q_pos[nq], k_pos[nk]: global token positions (used only when causal != 0)
+ * q_seg[nq], k_seg[nk]: sequence ids of packed sequences, or both NULL
  * o:    [nq, H, d] double;  lse: [nq, H] double
  * Returns 0, -1 when a scratch allocation fails, -2 when Hkv does not divide H.
  */
 int oracle_attention_fp64(const uint16_t *q, int64_t q_stride, const int64_t *q_pos, int64_t nq,
                           const uint16_t *k, const uint16_t *v, int64_t kv_stride,
                           const int64_t *k_pos, int64_t nk,
+                          const int64_t *q_seg, const int64_t *k_seg,
                           int H, int Hkv, int d, double scale, int causal,
                           double *o, double *lse, int nthreads) {
     int failed = 0;
@@ -85,6 +92,7 @@ int oracle_attention_fp64(const uint16_t *q, int64_t q_stride, const int64_t *q_
                 int64_t n_allowed = 0;
                 for (int64_t ik = 0; ik < nk; ++ik) {
                     if (causal && k_pos[ik] > q_pos[iq]) { s[ik] = -INFINITY; continue; }
+                    if (q_seg && k_seg[ik] != q_seg[iq]) { s[ik] = -INFINITY; continue; }
                     const uint16_t *kp = k + ik * kv_stride + (int64_t)(h / group) * d;
                     double dot = 0.0;
                     for (int e = 0; e < d; ++e) dot += qrow[e] * bf16_to_double(kp[e]);

@@ -42,6 +42,8 @@ SIGNATURES = {
                                    _F, _P, _SZ, _P]),
     "ra_ring_attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _F, _U,
                                   _P, _SZ, _P]),
+    "ra_ring_attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _I, _I, _F,
+                                     _U, _P, _SZ, _P]),
     "ra_ring_attn_fwd_stepwise_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I,
                                                _F, _P]),
     "ra_check_status": (_I, [_P, _P]),
@@ -191,6 +193,24 @@ def ra_ring_attn_fwd_gqa(q, k, v, o, lse, B, L, H, H_kv, d, N, layout, causal, s
                                       int(bool(causal)), float(scale), int(flags),
                                       _ptr(workspace, "workspace"),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ra_ring_attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, L, H, H_kv, d, N, layout, causal, scale=0.0,
+                            flags=0, workspace=None, stream=None):
+    """Ring sweep over packed sequences; ``cu_seqlens`` is an int32 CUDA tensor of n_seqs + 1
+    boundaries (B = 1)."""
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16
+    assert o.dtype in (torch.float32, torch.bfloat16) and lse.dtype == torch.float32
+    assert cu_seqlens.dtype == torch.int32
+    if o.dtype == torch.bfloat16:
+        flags |= RA_FLAG_O_BF16
+    _check(lib().ra_ring_attn_fwd_varlen(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(o, "o"),
+                                         _ptr(lse, "lse"), _ptr(cu_seqlens, "cu_seqlens"),
+                                         cu_seqlens.numel() - 1, L, H, H_kv, d, N, _layout(layout),
+                                         int(bool(causal)), float(scale), int(flags),
+                                         _ptr(workspace, "workspace"),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def ra_check_status(workspace, stream=None):

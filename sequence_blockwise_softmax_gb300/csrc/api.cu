@@ -219,7 +219,7 @@ namespace {
 ra_status ring_attn(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                     int64_t L, int64_t H, int64_t H_kv, int d, int N, int layout, int causal,
                     float scale, unsigned flags, void *workspace, size_t workspace_bytes,
-                    void *stream) {
+                    void *stream, const int *cu_seqlens = nullptr, int n_seqs = 0) {
     if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_INJECT_STALL))
         return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
     if ((flags & RA_FLAG_INJECT_STALL) && (flags & RA_FLAG_STEPWISE))
@@ -259,6 +259,8 @@ ra_status ring_attn(const void *q, const void *k, const void *v, void *o, float 
     a.causal = causal;
     a.scale = scale;
     a.ring = true;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
     if (!(flags & RA_FLAG_STEPWISE)) {
         a.o = o;
         a.ring_step = -1;
@@ -309,6 +311,19 @@ ra_status ra_ring_attn_fwd_gqa(const void *q, const void *k, const void *v, void
                                void *workspace, size_t workspace_bytes, void *stream) {
     return ring_attn(q, k, v, o, lse, B, L, H, H_kv, d, N, layout, causal, scale, flags, workspace,
                      workspace_bytes, stream);
+}
+
+ra_status ra_ring_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  const int32_t *cu_seqlens, int n_seqs, int64_t L, int64_t H,
+                                  int64_t H_kv, int d, int N, int layout, int causal, float scale,
+                                  unsigned flags, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (n_seqs < 1) return fail(RA_ERR_SHAPE, "n_seqs must be at least 1");
+    if (L > 0 && (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+        return fail(RA_ERR_INVALID_ARG, "cu_seqlens must be a 4-byte-aligned device pointer");
+    if (L >= ((int64_t)1 << 31)) return fail(RA_ERR_UNSUPPORTED, "packed length must fit in int32");
+    return ring_attn(q, k, v, o, lse, 1, L, H, H_kv, d, N, layout, causal, scale, flags, workspace,
+                     workspace_bytes, stream, cu_seqlens, n_seqs);
 }
 
 ra_status ra_check_status(void *workspace, void *stream) {

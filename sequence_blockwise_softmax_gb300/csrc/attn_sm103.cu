@@ -54,6 +54,8 @@ struct AttnArgs {
     int n_units_seq;    // ceil(S / 256)
     int inject_stall;   // test hook: CTA 0 never loads its second K tile
     int kv_group;       // query heads per key/value head (1 without GQA)
+    const int *cu_seqlens;  // packed sequences: n_seqs + 1 boundaries, or null
+    int n_seqs;
 };
 
 // Global position of local token s on rank r (the layout formulas of the
@@ -78,26 +80,50 @@ __device__ __forceinline__ int64_t keys_upto(int layout, int j, int64_t p, int N
     return clamp64(p - (int64_t)j * C + 1, 0, C) + clamp64(p - (int64_t)(2 * N - 1 - j) * C + 1, 0, C);
 }
 
-// The sequence of (kv rank, key tile) pairs a unit visits.  Every role walks
-// it identically.
+// Packed variable-length sequences: the boundaries [start, end) of the
+// sequence holding global position p (binary search; every read stays inside
+// the n + 1 boundaries whatever they hold).  Without packing: [0, total).
+__device__ __forceinline__ void seq_bounds(const int *cu, int n, int64_t total, int64_t p,
+                                           int64_t &start, int64_t &end) {
+    if (!cu) {
+        start = 0;
+        end = total;
+        return;
+    }
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= p) lo = mid;
+        else hi = mid;
+    }
+    start = cu[lo];
+    end = cu[lo + 1];
+}
+
+// The sequence of (kv rank, key tile) pairs a unit visits.  The keys of
+// shard j its rows may see are the local interval
+// [keys_upto(j, lo_pos), keys_upto(j, hi_pos)): lo_pos is one before the
+// start of the first row's sequence, hi_pos the last row's position (causal)
+// or the end of its sequence minus one.  Every role walks it identically.
 struct TileWalk {
-    int step, tile, ntiles, j;
-    int num_steps, step_base, q_rank, kv_fixed, N, layout, causal, S;
-    int64_t last_pos;
+    int step, tile, tile_end, j;
+    int num_steps, step_base, q_rank, kv_fixed, N, layout, S;
+    int64_t lo_pos, hi_pos;
 
     __device__ void start_step() {
         while (step < num_steps) {
             j = kv_fixed >= 0 ? kv_fixed : ((q_rank - step - step_base) % N + N) % N;
-            const int64_t kc = causal ? keys_upto(layout, j, last_pos, N, S) : (int64_t)S;
-            ntiles = (int)((kc + 127) / 128);
-            tile = 0;
-            if (ntiles > 0) return;
+            const int64_t lo = keys_upto(layout, j, lo_pos, N, S);
+            const int64_t hi = keys_upto(layout, j, hi_pos, N, S);
+            tile = (int)(lo / 128);
+            tile_end = (int)((hi + 127) / 128);
+            if (tile_end > tile) return;
             ++step;
         }
     }
     __device__ bool valid() const { return step < num_steps; }
     __device__ void next() {
-        if (++tile >= ntiles) {
+        if (++tile >= tile_end) {
             ++step;
             start_step();
         }
@@ -186,9 +212,17 @@ __global__ void __launch_bounds__(384, 1)
     walk0.kv_fixed = args.kv_rank_fixed;
     walk0.N = N;
     walk0.layout = args.layout;
-    walk0.causal = args.causal;
     walk0.S = S;
-    walk0.last_pos = token_pos(args.layout, q_rank, row_end - 1, N, S);
+    {
+        const int64_t total = (int64_t)N * S;
+        const int64_t first_pos = token_pos(args.layout, q_rank, row0, N, S);
+        const int64_t last_pos = token_pos(args.layout, q_rank, row_end - 1, N, S);
+        int64_t first_start, first_end, last_start, last_end;
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, first_start, first_end);
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, last_start, last_end);
+        walk0.lo_pos = first_start - 1;
+        walk0.hi_pos = args.causal ? last_pos : last_end - 1;
+    }
 
     // ---- setup
     if (threadIdx.x == 0) {
@@ -397,16 +431,21 @@ __global__ void __launch_bounds__(384, 1)
         float m_ref = -INFINITY;  // running max, already scaled to log2 units
         float l = 0.f;            // running denominator, relative to m_ref
         float lr = 0.f;           // the same sum over the bf16-rounded P the MMA uses
+        int64_t my_start, my_end;
+        seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, my_pos, my_start, my_end);
+        const int64_t my_lo_pos = my_start - 1;
+        const int64_t my_hi_pos = args.causal ? my_pos : my_end - 1;
         TileWalk w = walk0;
         w.start_step();
         int t = 0;
         bool ok = true;
-        int cur_j = -1;
-        int kc = S;
+        int cur_step = -1;
+        int klo = 0, khi = S;   // this row's visible local keys [klo, khi) of shard w.j
         for (; w.valid(); w.next(), ++t) {
-            if (w.j != cur_j || w.tile == 0) {
-                cur_j = w.j;
-                kc = args.causal ? (int)keys_upto(args.layout, w.j, my_pos, N, S) : S;
+            if (w.step != cur_step) {
+                cur_step = w.step;
+                klo = (int)keys_upto(args.layout, w.j, my_lo_pos, N, S);
+                khi = (int)keys_upto(args.layout, w.j, my_hi_pos, N, S);
             }
             if (!(ok = warp_wait(BAR(B_SFULL + g), t & 1, abort_flag))) break;
             tc_fence_after();
@@ -415,11 +454,12 @@ __global__ void __launch_bounds__(384, 1)
             for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
             tmem_wait_ld();
             float *s = reinterpret_cast<float *>(&sr[0][0]);
-            const int lim = kc - w.tile * 128;        // valid key columns for this row
-            if (lim < 128) {
+            const int lim = khi - w.tile * 128;       // columns [lim_lo, lim) are visible
+            const int lim_lo = klo - w.tile * 128;
+            if (lim < 128 || lim_lo > 0) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c >= lim) s[c] = -INFINITY;
+                    if (c >= lim || c < lim_lo) s[c] = -INFINITY;
             }
             // row max: four independent three-input chains
             float mA = s[0], mB = s[1], mC = s[2], mD = s[3];
@@ -629,6 +669,8 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     args.n_units_seq = (int)((a.S + 255) / 256);
     args.inject_stall = a.inject_stall ? 1 : 0;
     args.kv_group = (int)(a.H / (a.H_kv > 0 ? a.H_kv : a.H));
+    args.cu_seqlens = a.cu_seqlens;
+    args.n_seqs = a.n_seqs;
     const int64_t Zq = a.ring ? a.N * a.B : a.B;
     const int64_t Zkv = Zq;
     const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;

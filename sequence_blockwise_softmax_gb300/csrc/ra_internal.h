@@ -29,6 +29,8 @@ struct AttnLaunch {
     int ring_step;        // ring mode: -1 sweeps all N steps; s >= 0 runs step s only
     bool out_f32;
     bool inject_stall;    // test hook, see RA_FLAG_INJECT_STALL
+    const int *cu_seqlens;  // packed sequences (device, n_seqs + 1 boundaries), or null
+    int n_seqs;
 };
 
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);

@@ -84,3 +84,13 @@ def random_ints(n, low, high, seed):
 def random_perm(n, seed):
     g = torch.Generator().manual_seed(int(seed))
     return torch.randperm(n, generator=g)
+
+
+def make_cu_seqlens(L, n_seqs, seed):
+    """Boundaries of n_seqs packed sequences over L tokens: n_seqs - 1 distinct cut points
+    drawn uniformly from 1..L-1 with a seeded generator (a broad length mix, from a few
+    tokens to several times the mean).  Returns an int64 tensor [0, c_1, ..., L]."""
+    g = torch.Generator().manual_seed(int(seed))
+    cuts = torch.randperm(L - 1, generator=g)[:n_seqs - 1] + 1
+    return torch.cat([torch.zeros(1, dtype=torch.int64), cuts.sort().values,
+                      torch.full((1,), L, dtype=torch.int64)])

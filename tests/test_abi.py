@@ -103,6 +103,22 @@ def test_gqa_rejects_bad_head_counts_on_host(ralib):
     assert st == 2
 
 
+def test_varlen_rejects_bad_arguments(ralib):
+    lib = ralib.lib()
+    V = lambda cu, n: lib.ra_ring_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, n, 1024, 2, 2, 128, 4,
+                                                  0, 1, 0.0, 0, FAKE, 256, None)
+    assert V(FAKE, 0) == 2          # no sequences
+    assert V(0, 3) == 1             # no boundaries
+    assert V(FAKE + 2, 3) == 1      # misaligned boundaries
+
+
+def test_cu_seqlens_recipe():
+    from synthetic_inputs import make_cu_seqlens
+    cu = make_cu_seqlens(1000, 17, seed=3)
+    assert cu[0] == 0 and cu[-1] == 1000 and len(cu) == 18
+    assert bool((cu[1:] > cu[:-1]).all())
+
+
 def test_workspace_sizes(ralib):
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 0) == 256
     n = 1 * 1024 * 2 * 128

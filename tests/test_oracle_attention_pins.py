@@ -194,3 +194,46 @@ def test_gqa_rejects_bad_head_counts(ora):
     k = randn_bf16((3, 2, 4), 2)
     with pytest.raises((ValueError, AssertionError)):
         ora.attention(q, k, k)
+
+
+# --- packed variable-length sequences ---------------------------------------------------
+
+def test_varlen_single_token_sequences(ora):
+    """Every token its own sequence: O_t = v_t and LSE_t = scale * q_t . k_t, causal or not."""
+    L, H, d = 6, 2, 8
+    q, k, v = randn_bf16((1, L, H, d), 61), randn_bf16((1, L, H, d), 62), randn_bf16((1, L, H, d), 63)
+    for causal in (False, True):
+        o, lse = ora.full_attention(q, k, v, causal=causal, cu_seqlens=np.arange(L + 1))
+        np.testing.assert_allclose(o[0], v[0].double().numpy(), rtol=0, atol=1e-15)
+        qk = (q[0].double() * k[0].double()).sum(-1).numpy() / math.sqrt(d)
+        np.testing.assert_allclose(lse[0], qk.T, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_separate_sequences(ora, causal):
+    """Packed attention equals attention run on each sequence on its own, stitched back;
+    empty sequences are allowed."""
+    L, H, d = 40, 2, 16
+    cu = np.array([0, 7, 7, 19, 20, 40])
+    q, k, v = randn_bf16((1, L, H, d), 71), randn_bf16((1, L, H, d), 72), randn_bf16((1, L, H, d), 73)
+    o, lse = ora.full_attention(q, k, v, causal=causal, cu_seqlens=cu)
+    for a, b in zip(cu[:-1], cu[1:]):
+        if a == b:
+            continue
+        o_s, lse_s = ora.full_attention(q[:, a:b], k[:, a:b], v[:, a:b], causal=causal)
+        np.testing.assert_allclose(o[:, a:b], o_s, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, a:b], lse_s, rtol=0, atol=1e-13)
+
+
+def test_varlen_zero_queries_closed_form(ora):
+    """Q = 0, causal, packed: O_t is the mean of v over its own sequence up to t."""
+    L, H, d = 30, 1, 8
+    cu = np.array([0, 11, 12, 30])
+    q = torch.zeros((1, L, H, d), dtype=torch.bfloat16)
+    k, v = randn_bf16((1, L, H, d), 81), randn_bf16((1, L, H, d), 82)
+    o, lse = ora.full_attention(q, k, v, causal=True, cu_seqlens=cu)
+    vf = v.double().numpy()[0]
+    for t in range(L):
+        s0 = cu[np.searchsorted(cu, t, side="right") - 1]
+        np.testing.assert_allclose(o[0, t], vf[s0:t + 1].mean(axis=0), rtol=0, atol=1e-13)
+        assert lse[0, 0, t] == pytest.approx(math.log(t + 1 - s0), abs=1e-13)
