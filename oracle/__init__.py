@@ -17,6 +17,9 @@ Parts and what pins each (all pins live in ``tests/test_oracle_*.py``):
   * ``blockwise``: the online (m, l, O) recursion and the LSE merge -- pinned
     against one-shot attention under random block splits and orders, and by
     lse = m + ln l.
+  * ``backward``: fp64 gradients of attention -- pinned by central finite
+    differences of a separately written forward, and by the identities
+    sum_k dK = 0 and sum_k dV = sum_q dO (``tests/test_oracle_backward_pins.py``).
 """
 import ctypes
 import os
@@ -24,7 +27,7 @@ import subprocess
 
 import numpy as np
 
-from . import blockwise, layouts  # noqa: F401
+from . import backward, blockwise, layouts  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attention_fp64.c")
@@ -167,5 +170,5 @@ def block_attention(q_shard, k_shard, v_shard, layout, N, q_rank, kv_rank, causa
     return np.stack(outs), np.stack(lses)
 
 
-__all__ = ["attention", "full_attention", "block_attention", "blockwise", "layouts",
+__all__ = ["attention", "full_attention", "block_attention", "backward", "blockwise", "layouts",
            "build", "num_threads"]
