@@ -236,6 +236,32 @@ RA_API ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void *k,
                                                    int causal, float scale, void *stream);
 
 /*
+ * ra_ring_attn_bwd -- gradients of ra_ring_attn_fwd.  The pages describe the
+ * forward only; this is the plain derivative of softmax(Q K^T * scale) V
+ * under the same masks (causal by position, optional packed sequences,
+ * grouped key/value heads):
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  D = rowsum(dO * O),
+ *   dQ = dS K * scale,  dK = dS^T Q * scale,
+ * with P rebuilt from the forward's LSE.  Deterministic (no atomics): one
+ * pass over key tiles for dK and dV, one over query tiles for dQ.
+ * q: bf16 [N, B, S, H, d]; k, v: bf16 [N, B, S, H_kv, d]; o: fp32 forward
+ * output [N, B, S, H, d]; dout: bf16 gradient of O, like q; lse: fp32
+ * [N, B, H, S] from the forward.  dq: fp32 like q; dk, dv: fp32 like k.
+ * cu_seqlens / n_seqs: packed sequences as in ra_ring_attn_fwd_varlen (B = 1),
+ * or NULL / 0.  d in {64, 128}; workspace: ra_ring_attn_bwd_workspace_bytes()
+ * bytes (status word and D), zero-filled before its first use.
+ */
+RA_API ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const float *o,
+                                  const void *dout, const float *lse, float *dq, float *dk,
+                                  float *dv, const int32_t *cu_seqlens, int n_seqs, int64_t B,
+                                  int64_t L, int64_t H, int64_t H_kv, int d, int N, int layout,
+                                  int causal, float scale, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Workspace bytes ra_ring_attn_bwd needs (0 on bad arguments). */
+RA_API size_t ra_ring_attn_bwd_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N);
+
+/*
  * ra_check_status -- synchronise `stream`, read the status word at the start
  * of `workspace`, clear it, and return RA_ERR_TIMEOUT if a kernel recorded a
  * timeout since the last check (RA_OK otherwise).

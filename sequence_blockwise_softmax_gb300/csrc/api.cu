@@ -326,6 +326,66 @@ ra_status ra_ring_attn_fwd_varlen(const void *q, const void *k, const void *v, v
                      workspace_bytes, stream, cu_seqlens, n_seqs);
 }
 
+size_t ra_ring_attn_bwd_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N) {
+    if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
+    return kHeader + round256((size_t)B * (size_t)L * (size_t)H * 4);
+}
+
+ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const float *o,
+                           const void *dout, const float *lse, float *dq, float *dk, float *dv,
+                           const int32_t *cu_seqlens, int n_seqs, int64_t B, int64_t L, int64_t H,
+                           int64_t H_kv, int d, int N, int layout, int causal, float scale,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
+    if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
+    if (L % N) return fail(RA_ERR_SHAPE, "N must divide L");
+    if (layout == RA_ZIGZAG && (L % (2 * (int64_t)N))) return fail(RA_ERR_SHAPE, "zigzag needs 2N | L");
+    const int64_t S = L / N;
+    ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
+    if (st != RA_OK) return st;
+    if (H > 0 && (st = check_kv_heads(H, H_kv)) != RA_OK) return st;
+    if (cu_seqlens) {
+        if (B != 1) return fail(RA_ERR_SHAPE, "packed sequences need B = 1");
+        if (n_seqs < 1) return fail(RA_ERR_SHAPE, "n_seqs must be at least 1");
+        if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+            return fail(RA_ERR_ALIGNMENT, "cu_seqlens must be 4-byte aligned");
+    }
+    if (B * L * H == 0) return RA_OK;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return fail(RA_ERR_INVALID_ARG, "null pointer argument");
+    const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(RA_ERR_ALIGNMENT, "every tensor pointer must be 16-byte aligned");
+    if (workspace_bytes < ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N))
+        return fail(RA_ERR_INVALID_ARG, "workspace smaller than ra_ring_attn_bwd_workspace_bytes()");
+    ra::BwdLaunch a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dout = dout;
+    a.o = o;
+    a.lse = lse;
+    a.dvec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeader);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.status = static_cast<unsigned *>(workspace);
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.H_kv = H_kv;
+    a.d = d;
+    a.N = N;
+    a.layout = layout;
+    a.causal = causal;
+    a.scale = scale;
+    const char *err = nullptr;
+    st = ra::launch_attention_bwd(a, static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "backward launch failed");
+}
+
 ra_status ra_check_status(void *workspace, void *stream) {
     if (!workspace) return fail(RA_ERR_INVALID_ARG, "null workspace");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

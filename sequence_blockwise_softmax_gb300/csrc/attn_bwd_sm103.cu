@@ -1,0 +1,793 @@
+// attn_bwd_sm103.cu -- gradients of the ring attention on the sm_103a tensor cores.
+//
+// The pages give the forward pass only; these kernels differentiate it:
+// for one head, with P = softmax(S), S = Q K^T * scale under the forward's
+// masks, and dO the gradient of O,
+//     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O),
+//     dQ = dS K * scale,  dK = dS^T Q * scale.
+// P is rebuilt exactly from the forward's LSE: P = exp2(S * scale * log2 e -
+// LSE * log2 e); no online softmax is needed.
+//
+// Two passes, no atomics, deterministic:
+//   dot kernel   D = rowsum(dO * O), one warp per row, reduced by shuffles.
+//   pass A       one CTA per 128 keys of one (kv rank, batch, kv head):
+//                S^T = K Q^T and dP^T = V dO^T into tensor memory for each
+//                visible 128-query tile of every query rank and every query
+//                head of the group; one thread per key builds P^T and dS^T
+//                (bf16, back into tensor memory); dV += P^T dO and
+//                dK += dS^T Q accumulate in tensor memory.
+//   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
+//                visible key tile in ring order; one thread per query builds
+//                dS; dQ += dS K accumulates in tensor memory.
+// Masks (causal by position, packed sequences) are the forward's: in every
+// layout positions increase along a rank, so the visible partners of a row in
+// a shard form one interval of local indices.
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer
+// (elect.sync), warp 2 tensor-memory allocator, warps 4-7 the elementwise
+// warpgroup (thread = tensor-memory lane).  Every wait is bounded.
+#include <cmath>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+#include "ra_positions.cuh"
+
+namespace ra {
+
+struct BwdArgs {
+    const float *lse;       // [Z, H, S] natural log (forward output)
+    const float *dvec;      // [Z, H, S] D = rowsum(dO * O)
+    float *dq;              // [Z, S, H, d]
+    float *dk, *dv;         // [Z, S, H_kv, d]
+    unsigned *status;
+    const int *cu_seqlens;
+    int n_seqs;
+    int B, S, H, Hkv, N, layout, causal;
+    float scale, scale_log2;
+    int n_tiles_seq;        // ceil(S / 128)
+};
+
+__device__ __forceinline__ uint8_t *bwd_align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void bwd_timeout(unsigned *status, volatile int *abort) {
+    *abort = 1;
+    atomicOr(status, RA_DEV_TIMEOUT_BIT);
+}
+
+// S-style product: D[tmem] = A B^T over K = d, both operands K-major 128-row
+// tiles stored as 64-column boxes (offsets in 16-byte units).
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, 128, false);
+    mma_ss_elect<0, 0>(d_tmem, a0, b0, IDESC, 0u);
+    mma_ss_elect<2, 2>(d_tmem, a0, b0, IDESC, 1u);
+    mma_ss_elect<4, 4>(d_tmem, a0, b0, IDESC, 1u);
+    mma_ss_elect<6, 6>(d_tmem, a0, b0, IDESC, 1u);
+    if (D == 128) {
+        constexpr uint32_t h = (128u * 128u) >> 4;
+        mma_ss_elect<h, h>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<h + 2, h + 2>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<h + 4, h + 4>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<h + 6, h + 6>(d_tmem, a0, b0, IDESC, 1u);
+    }
+}
+
+// Accumulating product: D[tmem] (+)= A[tmem, bf16, 128 x 128] B[smem], B a
+// 128-row tile read MN-major (N = d), 16 rows per k-step.
+template <int D>
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, bool first) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, D, true);
+    mma_ts_elect<0, 0>(d_tmem, a_tmem, b0, IDESC, first ? 0u : 1u);
+    mma_ts_elect<8, 128>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<16, 256>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<24, 384>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<32, 512>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<40, 640>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<48, 768>(d_tmem, a_tmem, b0, IDESC, 1u);
+    mma_ts_elect<56, 896>(d_tmem, a_tmem, b0, IDESC, 1u);
+}
+
+// Write 32 accumulator columns of one row (scaled) as fp32.
+__device__ __forceinline__ void store_row32(float *dst, const uint32_t (&r)[32], float mul) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        d4[c] = make_float4(__uint_as_float(r[4 * c]) * mul, __uint_as_float(r[4 * c + 1]) * mul,
+                            __uint_as_float(r[4 * c + 2]) * mul, __uint_as_float(r[4 * c + 3]) * mul);
+}
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const uint16_t *dout, const float *o,
+                                                      float *dvec, int64_t rows, int H, int64_t S) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    constexpr int PER = D / 32;   // elements per lane
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const uint16_t *dp = dout + r * D + lane * PER;
+        const float *op = o + r * D + lane * PER;
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc += __uint_as_float((uint32_t)dp[e] << 16) * op[e];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            // row r = (z * S + s) * H + h  ->  D index (z * H + h) * S + s
+            const int64_t h = r % H, zs = r / H;
+            const int64_t s = zs % S, z = zs / S;
+            dvec[(z * H + h) * S + s] = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- pass B: dQ
+template <int D>
+struct BwdQSmem {
+    static constexpr int kStages = 2;
+    static constexpr uint32_t kTile = 128u * D * 2u;
+    static constexpr uint32_t kBox = 128u * 128u;
+    static constexpr uint32_t kQ = 0, kDO = kTile, kK = 2 * kTile;
+    static constexpr uint32_t kV = kK + kStages * kTile;
+    static constexpr uint32_t kBars = kV + kStages * kTile;
+    // Q+dO full, K full[2], V full[2], K empty[2], V empty[2], S full, dP full,
+    // dS full, dQ done, final
+    static constexpr int kNumBars = 1 + 4 * kStages + 5;
+    static constexpr uint32_t kMisc = kBars + kNumBars * 8;
+    static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                       const BwdArgs args) {
+    using L = BwdQSmem<D>;
+    constexpr int NS = L::kStages;
+    constexpr int HALVES = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = bwd_align1024(smem_raw);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + L::kBars;
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KEMPTY = 1 + 2 * NS, B_VEMPTY = 1 + 3 * NS,
+              B_SFULL = 1 + 4 * NS, B_DPFULL = B_SFULL + 1, B_DSFULL = B_SFULL + 2,
+              B_DQDONE = B_SFULL + 3, B_FINAL = B_SFULL + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int S = args.S, H = args.H, N = args.N;
+    const int per_bh = N * args.n_tiles_seq;
+    const int bh = blockIdx.x / per_bh, rem = blockIdx.x % per_bh;
+    const int b = bh / H, h = bh % H;
+    const int qi = rem / args.n_tiles_seq, qt = rem % args.n_tiles_seq;
+    const int zq = qi * args.B + b;
+    const int row0 = qt * 128;
+    const int row_end = min(S, row0 + 128);
+    const int hk = h / (H / args.Hkv);
+    const int64_t total = (int64_t)N * S;
+
+    TileWalk walk0;
+    walk0.step = 0;
+    walk0.num_steps = N;
+    walk0.step_base = 0;
+    walk0.q_rank = qi;
+    walk0.kv_fixed = -1;
+    walk0.N = N;
+    walk0.layout = args.layout;
+    walk0.S = S;
+    {
+        const int64_t first_pos = token_pos(args.layout, qi, row0, N, S);
+        const int64_t last_pos = token_pos(args.layout, qi, row_end - 1, N, S);
+        int64_t fs, fe, ls, le;
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, fs, fe);
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, ls, le);
+        walk0.lo_pos = fs - 1;
+        walk0.hi_pos = args.causal ? last_pos : le - 1;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_QFULL), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(B_KFULL + s), 1);
+            mbar_init(BAR(B_VFULL + s), 1);
+            mbar_init(BAR(B_KEMPTY + s), 1);
+            mbar_init(BAR(B_VEMPTY + s), 1);
+        }
+        mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_DPFULL), 1);
+        mbar_init(BAR(B_DSFULL), 128);
+        mbar_init(BAR(B_DQDONE), 1);
+        mbar_init(BAR(B_FINAL), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        int t = 0, k_issued = 0, v_issued = 0;
+        bool ok = true;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
+            for (int c = 0; c < HALVES; ++c) {
+                tma_load_3d(s_base + L::kQ + c * L::kBox, &tmq, BAR(B_QFULL), h * D + 64 * c, row0, zq);
+                tma_load_3d(s_base + L::kDO + c * L::kBox, &tmdo, BAR(B_QFULL), h * D + 64 * c, row0, zq);
+            }
+        }
+        __syncwarp();
+        TileWalk w = walk0;
+        w.start_step();
+        for (; w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            const int zkv = w.j * args.B + b, y = w.tile * 128;
+            if (t >= NS && !(ok = warp_wait(BAR(B_KEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
+                for (int c = 0; c < HALVES; ++c)
+                    tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
+                                hk * D + 64 * c, y, zkv);
+            }
+            __syncwarp();
+            k_issued = t + 1;
+            if (t >= NS && !(ok = warp_wait(BAR(B_VEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
+                for (int c = 0; c < HALVES; ++c)
+                    tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
+                                hk * D + 64 * c, y, zkv);
+            }
+            __syncwarp();
+            v_issued = t + 1;
+        }
+        if (!ok) {
+            if (lane == 0) bwd_timeout(args.status, abort_flag);
+            volatile int never = 0;
+            mbar_wait(BAR(B_QFULL), 0, &never);
+            for (int u = (k_issued > NS ? k_issued - NS : 0); u < k_issued; ++u)
+                mbar_wait(BAR(B_KFULL + u % NS), (u / NS) & 1, &never);
+            for (int u = (v_issued > NS ? v_issued - NS : 0); u < v_issued; ++u)
+                mbar_wait(BAR(B_VFULL + u % NS), (u / NS) & 1, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        const uint64_t dq_desc = sdesc_sw128(s_base + L::kQ, 16, 1024);
+        const uint64_t ddo_desc = sdesc_sw128(s_base + L::kDO, 16, 1024);
+        const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);       // K as K-major operand
+        const uint64_t dk_mn = sdesc_sw128(s_base + L::kK, L::kBox, 1024); // K as MN-major operand
+        const uint64_t dv_k = sdesc_sw128(s_base + L::kV, 16, 1024);
+        bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
+        TileWalk w = walk0;
+        w.start_step();
+        int t = 0;
+        for (; ok && w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            const uint32_t ph = (t / NS) & 1;
+            const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
+            if (!(ok = warp_wait(BAR(B_KFULL + st), ph, abort_flag))) break;
+            // dS of the previous tile (in the S columns) must be consumed
+            if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE), (t - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_kmajor<D>(tmem, dq_desc, dk_k + soff);                 // S = Q K^T
+            tc_commit_elect(BAR(B_SFULL));
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
+            tc_fence_after();
+            issue_kmajor<D>(tmem + 128, ddo_desc, dv_k + soff);          // dP = dO V^T
+            tc_commit_elect(BAR(B_DPFULL));
+            tc_commit_elect(BAR(B_VEMPTY + st));
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_ts<D>(tmem + 256, tmem, dk_mn + soff, t == 0);          // dQ += dS K
+            tc_commit_elect(BAR(B_DQDONE));
+            tc_commit_elect(BAR(B_KEMPTY + st));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+        __syncwarp();
+        tc_commit_elect(BAR(B_FINAL));
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(BAR(B_FINAL), 0, &never);
+    } else if (warp >= 4) {
+        // ------------------------------------------------ dS, one thread per query row
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int a = row0 + r;
+        const int a_c = a < S ? a : S - 1;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128, tQ = tmem + lane_off + 256;
+        const int64_t my_pos = token_pos(args.layout, qi, a_c, N, S);
+        int64_t my_start, my_end;
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, my_pos, my_start, my_end);
+        const int64_t lo_pos = my_start - 1, hi_pos = args.causal ? my_pos : my_end - 1;
+        const size_t vi = ((size_t)zq * H + h) * S + a_c;
+        const float lse2 = args.lse[vi] * 1.4426950408889634f;
+        const float dval = args.dvec[vi];
+        const float sl2 = args.scale_log2;
+        TileWalk w = walk0;
+        w.start_step();
+        int t = 0, cur_step = -1, klo = 0, khi = S;
+        bool ok = true;
+        for (; w.valid(); w.next(), ++t) {
+            if (w.step != cur_step) {
+                cur_step = w.step;
+                klo = (int)keys_upto(args.layout, w.j, lo_pos, N, S);
+                khi = (int)keys_upto(args.layout, w.j, hi_pos, N, S);
+            }
+            if (!(ok = warp_wait(BAR(B_SFULL), t & 1, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
+            tc_fence_after();
+            const int lim = khi - w.tile * 128, lim_lo = klo - w.tile * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t sv[32], pv[32];
+                tmem_ld32(tS + 32 * q, sv);
+                tmem_ld32(tP + 32 * q, pv);
+                tmem_wait_ld();
+                uint32_t out[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const int col = 32 * q + c;
+                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
+                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2));
+                    if (col >= lim || col < lim_lo) p0 = 0.f;
+                    if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
+                    out[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - dval),
+                                              p1 * (__uint_as_float(pv[c + 1]) - dval));
+                }
+                tmem_st16(tS + 16 * q, out);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_DSFULL));
+        }
+        if (!ok) {
+            if (lane == 0) bwd_timeout(args.status, abort_flag);
+        } else {
+            const int T = t;
+            if (T > 0) {
+                ok = warp_wait(BAR(B_DQDONE), (T - 1) & 1, abort_flag);
+                if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+                tc_fence_after();
+            }
+            // tensor-memory loads are warp-wide; only the stores depend on the row
+            if (ok) {
+                float *dst = args.dq + (((size_t)zq * S + a_c) * H + h) * D;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t v[32];
+                    if (T > 0) {
+                        tmem_ld32(tQ + 32 * q, v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] = 0u;
+                    }
+                    if (a < S) store_row32(dst + 32 * q, v, args.scale);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- pass A: dK, dV
+template <int D>
+struct BwdKVSmem {
+    static constexpr int kStages = 2;
+    static constexpr uint32_t kTile = 128u * D * 2u;
+    static constexpr uint32_t kBox = 128u * 128u;
+    static constexpr uint32_t kK = 0, kV = kTile;
+    static constexpr uint32_t kQ = 2 * kTile;
+    static constexpr uint32_t kDO = kQ + kStages * kTile;
+    static constexpr uint32_t kVec = kDO + kStages * kTile;       // per stage: lse2[128], D[128]
+    static constexpr uint32_t kBars = kVec + kStages * 1024;
+    // K+V full, Q full[2], Q empty[2], S full, dP full, P full, MMA done, final
+    static constexpr int kNumBars = 1 + 2 * kStages + 5;
+    static constexpr uint32_t kMisc = kBars + kNumBars * 8;
+    static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+};
+
+// The query tiles a block of keys meets, for each query head of its group and
+// each query rank in ring order (j, j+1, ...): for keys at positions
+// first_pos..last_pos the visible queries of rank i are the local interval
+// [keys_upto(i, lo_pos), keys_upto(i, hi_pos)).
+struct QWalk {
+    int head, step, tile, tile_end, i;
+    int heads, N, j, layout, S;
+    int64_t lo_pos, hi_pos;
+
+    __device__ void start() {
+        while (head < heads) {
+            while (step < N) {
+                i = (j + step) % N;
+                const int64_t lo = keys_upto(layout, i, lo_pos, N, S);
+                const int64_t hi = keys_upto(layout, i, hi_pos, N, S);
+                tile = (int)(lo / 128);
+                tile_end = (int)((hi + 127) / 128);
+                if (tile_end > tile) return;
+                ++step;
+            }
+            step = 0;
+            ++head;
+        }
+    }
+    __device__ bool valid() const { return head < heads; }
+    __device__ void next() {
+        if (++tile >= tile_end) {
+            ++step;
+            start();
+        }
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                        const BwdArgs args) {
+    using L = BwdKVSmem<D>;
+    constexpr int NS = L::kStages;
+    constexpr int HALVES = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = bwd_align1024(smem_raw);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + L::kBars;
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    const int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS, B_DPFULL = B_SFULL + 1,
+              B_PFULL = B_SFULL + 2, B_MMADONE = B_SFULL + 3, B_FINAL = B_SFULL + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int S = args.S, H = args.H, N = args.N, Hkv = args.Hkv;
+    const int group = H / Hkv;
+    const int per_bh = N * args.n_tiles_seq;
+    const int bh = blockIdx.x / per_bh, rem = blockIdx.x % per_bh;
+    const int b = bh / Hkv, hk = bh % Hkv;
+    const int kj = rem / args.n_tiles_seq, kt = rem % args.n_tiles_seq;
+    const int zk = kj * args.B + b;
+    const int c0 = kt * 128;
+    const int c_end = min(S, c0 + 128);
+    const int64_t total = (int64_t)N * S;
+
+    QWalk walk0;
+    walk0.head = 0;
+    walk0.step = 0;
+    walk0.heads = group;
+    walk0.N = N;
+    walk0.j = kj;
+    walk0.layout = args.layout;
+    walk0.S = S;
+    {
+        const int64_t first_pos = token_pos(args.layout, kj, c0, N, S);
+        const int64_t last_pos = token_pos(args.layout, kj, c_end - 1, N, S);
+        int64_t fs, fe, ls, le;
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, fs, fe);
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, ls, le);
+        walk0.lo_pos = args.causal ? first_pos - 1 : fs - 1;
+        walk0.hi_pos = le - 1;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_KVFULL), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(B_QFULL + s), 33);    // the TMA arrival + 32 lanes storing lse2 / D
+            mbar_init(BAR(B_QEMPTY + s), 1);
+        }
+        mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_DPFULL), 1);
+        mbar_init(BAR(B_PFULL), 128);
+        mbar_init(BAR(B_MMADONE), 1);
+        mbar_init(BAR(B_FINAL), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        bool ok = true;
+        int t = 0, issued = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(BAR(B_KVFULL), 2 * L::kTile);
+            for (int c = 0; c < HALVES; ++c) {
+                tma_load_3d(s_base + L::kK + c * L::kBox, &tmk, BAR(B_KVFULL), hk * D + 64 * c, c0, zk);
+                tma_load_3d(s_base + L::kV + c * L::kBox, &tmv, BAR(B_KVFULL), hk * D + 64 * c, c0, zk);
+            }
+        }
+        __syncwarp();
+        QWalk w = walk0;
+        w.start();
+        for (; w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            const int h = hk * group + w.head;
+            const int zq = w.i * args.B + b, y = w.tile * 128;
+            if (t >= NS && !(ok = warp_wait(BAR(B_QEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(B_QFULL + st), 2 * L::kTile);
+                for (int c = 0; c < HALVES; ++c) {
+                    tma_load_3d(s_base + L::kQ + st * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL + st),
+                                h * D + 64 * c, y, zq);
+                    tma_load_3d(s_base + L::kDO + st * L::kTile + c * L::kBox, &tmdo, BAR(B_QFULL + st),
+                                h * D + 64 * c, y, zq);
+                }
+            }
+            // lse2 and D of the 128 query rows (0 past the shard's end)
+            float *vec = reinterpret_cast<float *>(smem + L::kVec + st * 1024);
+            const size_t base = ((size_t)zq * H + h) * S;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = y + lane * 4 + e;
+                vec[lane * 4 + e] = row < S ? args.lse[base + row] * 1.4426950408889634f : 0.f;
+                vec[128 + lane * 4 + e] = row < S ? args.dvec[base + row] : 0.f;
+            }
+            mbar_arrive(BAR(B_QFULL + st));
+            __syncwarp();
+            issued = t + 1;
+        }
+        if (!ok) {
+            if (lane == 0) bwd_timeout(args.status, abort_flag);
+            volatile int never = 0;
+            mbar_wait(BAR(B_KVFULL), 0, &never);
+            for (int u = (issued > NS ? issued - NS : 0); u < issued; ++u)
+                mbar_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);
+        const uint64_t dv_k = sdesc_sw128(s_base + L::kV, 16, 1024);
+        const uint64_t dq_k = sdesc_sw128(s_base + L::kQ, 16, 1024);
+        const uint64_t ddo_k = sdesc_sw128(s_base + L::kDO, 16, 1024);
+        const uint64_t dq_mn = sdesc_sw128(s_base + L::kQ, L::kBox, 1024);
+        const uint64_t ddo_mn = sdesc_sw128(s_base + L::kDO, L::kBox, 1024);
+        bool ok = warp_wait(BAR(B_KVFULL), 0, abort_flag);
+        QWalk w = walk0;
+        w.start();
+        int t = 0;
+        for (; ok && w.valid(); w.next(), ++t) {
+            const int st = t % NS;
+            const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
+            if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
+            if (t > 0 && !(ok = warp_wait(BAR(B_MMADONE), (t - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_kmajor<D>(tmem, dk_k, dq_k + soff);            // S^T = K Q^T
+            tc_commit_elect(BAR(B_SFULL));
+            issue_kmajor<D>(tmem + 128, dv_k, ddo_k + soff);     // dP^T = V dO^T
+            tc_commit_elect(BAR(B_DPFULL));
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_ts<D>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
+            issue_ts<D>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
+            tc_commit_elect(BAR(B_MMADONE));
+            tc_commit_elect(BAR(B_QEMPTY + st));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+        __syncwarp();
+        tc_commit_elect(BAR(B_FINAL));
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(BAR(B_FINAL), 0, &never);
+    } else if (warp >= 4) {
+        // ------------------------------------------------ P^T, dS^T, one thread per key
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int kk = c0 + r;
+        const int kk_c = kk < S ? kk : S - 1;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128;
+        const uint32_t tV = tmem + lane_off + 256, tK = tmem + lane_off + 256 + D;
+        const int64_t kpos = token_pos(args.layout, kj, kk_c, N, S);
+        int64_t ks, ke;
+        seq_bounds(args.cu_seqlens, args.n_seqs, total, kpos, ks, ke);
+        const int64_t lo_pos = args.causal ? kpos - 1 : ks - 1, hi_pos = ke - 1;
+        const float sl2 = args.scale_log2;
+        QWalk w = walk0;
+        w.start();
+        int t = 0, cur = -1, qlo = 0, qhi = S;
+        bool ok = true;
+        for (; w.valid(); w.next(), ++t) {
+            if (w.step != cur) {
+                cur = w.step;
+                qlo = (int)keys_upto(args.layout, w.i, lo_pos, N, S);
+                qhi = (int)keys_upto(args.layout, w.i, hi_pos, N, S);
+            }
+            const int st = t % NS;
+            if (!(ok = warp_wait(BAR(B_SFULL), t & 1, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
+            // the lse2 / D vectors of this tile (stored before the QFULL arrivals)
+            if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
+            tc_fence_after();
+            const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 1024);
+            const int lim = qhi - w.tile * 128, lim_lo = qlo - w.tile * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t sv[32], pv[32];
+                tmem_ld32(tS + 32 * q, sv);
+                tmem_ld32(tP + 32 * q, pv);
+                tmem_wait_ld();
+                uint32_t outp[16], outs[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const int col = 32 * q + c;
+                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -vec[col]));
+                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -vec[col + 1]));
+                    if (col >= lim || col < lim_lo) p0 = 0.f;
+                    if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
+                    outp[c >> 1] = pack_bf16x2(p0, p1);
+                    outs[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - vec[128 + col]),
+                                               p1 * (__uint_as_float(pv[c + 1]) - vec[128 + col + 1]));
+                }
+                tmem_st16(tS + 16 * q, outp);
+                tmem_st16(tP + 16 * q, outs);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_PFULL));
+        }
+        if (!ok) {
+            if (lane == 0) bwd_timeout(args.status, abort_flag);
+        } else {
+            const int T = t;
+            if (T > 0) {
+                ok = warp_wait(BAR(B_MMADONE), (T - 1) & 1, abort_flag);
+                if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+                tc_fence_after();
+            }
+            // tensor-memory loads are warp-wide; only the stores depend on the row
+            if (ok) {
+                const size_t row = (((size_t)zk * S + kk_c) * Hkv + hk) * D;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t v[32];
+                    if (T > 0) {
+                        tmem_ld32(tV + 32 * q, v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] = 0u;
+                    }
+                    if (kk < S) store_row32(args.dv + row + 32 * q, v, 1.f);
+                    if (T > 0) {
+                        tmem_ld32(tK + 32 * q, v);
+                        tmem_wait_ld();
+                    }
+                    if (kk < S) store_row32(args.dk + row + 32 * q, v, args.scale);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- host
+typedef CUresult (*BwdEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static BwdEncodeFn bwd_encode_fn() {
+    static BwdEncodeFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<BwdEncodeFn>(p);
+    }
+    return fn;
+}
+
+static bool bwd_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d) {
+    BwdEncodeFn enc = bwd_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)(H * d), (cuuint64_t)S, (cuuint64_t)Z};
+    cuuint64_t strides[2] = {(cuuint64_t)(H * d * 2), (cuuint64_t)(S * H * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t stream, const char **err) {
+    const int64_t Z = (int64_t)a.N * a.B;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!bwd_map(&mq, a.q, Z, a.S, a.H, D) || !bwd_map(&mk, a.k, Z, a.S, a.H_kv, D) ||
+        !bwd_map(&mv, a.v, Z, a.S, a.H_kv, D) || !bwd_map(&mdo, a.dout, Z, a.S, a.H, D)) {
+        *err = "cuTensorMapEncodeTiled failed for the backward tensor maps";
+        return RA_ERR_CUDA;
+    }
+    // D = rowsum(dO * O)
+    {
+        const int64_t rows = Z * a.S * a.H;
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int64_t blocks = (rows + 7) / 8;
+        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+        bwd_dot_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(a.dout), a.o,
+                                                                 a.dvec, rows, (int)a.H, a.S);
+    }
+    auto kq = attn_bwd_dq_kernel<D>;
+    auto kkv = attn_bwd_dkv_kernel<D>;
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdQSmem<D>::kBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdKVSmem<D>::kBytes) !=
+            cudaSuccess) {
+        *err = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+        return RA_ERR_CUDA;
+    }
+    const int64_t grid_kv = Z * a.H_kv * args.n_tiles_seq;
+    const int64_t grid_q = Z * a.H * args.n_tiles_seq;
+    if (grid_kv > 0x7fffffffLL || grid_q > 0x7fffffffLL) {
+        *err = "too many tiles for one launch";
+        return RA_ERR_UNSUPPORTED;
+    }
+    kkv<<<(unsigned)grid_kv, 256, BwdKVSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
+    kq<<<(unsigned)grid_q, 256, BwdQSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = cudaGetErrorString(e);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
+ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const char **err) {
+    BwdArgs args;
+    args.lse = a.lse;
+    args.dvec = a.dvec;
+    args.dq = a.dq;
+    args.dk = a.dk;
+    args.dv = a.dv;
+    args.status = a.status;
+    args.cu_seqlens = a.cu_seqlens;
+    args.n_seqs = a.n_seqs;
+    args.B = (int)a.B;
+    args.S = (int)a.S;
+    args.H = (int)a.H;
+    args.Hkv = (int)a.H_kv;
+    args.N = a.N;
+    args.layout = a.layout;
+    args.causal = a.causal ? 1 : 0;
+    args.scale = a.scale > 0.f ? a.scale : 1.0f / std::sqrt((float)a.d);
+    args.scale_log2 = args.scale * 1.4426950408889634f;
+    args.n_tiles_seq = (int)((a.S + 127) / 128);
+    if ((int64_t)a.N * a.B * a.S * a.H == 0) return RA_OK;
+    return a.d == 128 ? bwd_launch_t<128>(a, args, stream, err) : bwd_launch_t<64>(a, args, stream, err);
+}
+
+}  // namespace ra

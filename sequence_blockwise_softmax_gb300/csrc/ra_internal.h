@@ -35,6 +35,25 @@ struct AttnLaunch {
 
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);
 
+// One backward: D = rowsum(dO * O), then the dK / dV pass and the dQ pass.
+// q, dout: bf16 [N, B, S, H, d]; k, v: bf16 [N, B, S, H_kv, d]; o: fp32
+// [N, B, S, H, d]; lse, dvec: fp32 [N, B, H, S]; dq: fp32 like q; dk, dv:
+// fp32 like k.
+struct BwdLaunch {
+    const void *q, *k, *v, *dout;
+    const float *o, *lse;
+    float *dvec;
+    float *dq, *dk, *dv;
+    unsigned *status;
+    const int *cu_seqlens;
+    int n_seqs;
+    int64_t B, S, H, H_kv;
+    int d, N, layout, causal;
+    float scale;
+};
+
+ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const char **err);
+
 ra_status launch_permute(const void *src, void *dst, int op, int layout, int64_t B, int64_t L,
                          int64_t H, int64_t d, int R, int U, int elem_bytes, cudaStream_t stream,
                          const char **err);
