@@ -38,6 +38,7 @@ import torch  # noqa: E402
 from synthetic_inputs import WORKLOADS, make_cu_seqlens, make_qkv  # noqa: E402
 
 METRIC = "causal ring-attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
+METRIC_BWD = "causal ring-attention bwd TFLOP/s (bf16, 1×GB300; algorithmic 8·B·H·d·pairs)"
 DEFAULT_WORKLOAD = "striped_B1_H8_L131072_d128_N16"
 LAUNCHES_PER_STEP = 6          # 3 shard permutes, 1 ring sweep, 1 O un-permute, 1 LSE un-permute
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_striped_128k_traffic.txt")
@@ -227,6 +228,42 @@ class Workload:
         ra.ra_shard_permute(o, self.o_seq, ra.RA_SHARDS_TO_SEQ, self.layout, B, L, H, d, N, U)
         ra.ra_lse_to_seq(self.lse_ring, self.lse_seq, self.layout, B, L, H, N, U)
 
+    def prepare_backward(self):
+        """Forward once (saved activations), then buffers for the backward step."""
+        ra, B, L, H, d, N = self.ra, self.B, self.L, self.H, self.d, self.N
+        if self.U != 1 or self.cu is not None:
+            raise ValueError("the backward bench runs plain ring layouts")
+        self.step()
+        g = torch.Generator().manual_seed(7)
+        do = torch.randn((B, L, H, d), generator=g).to(torch.bfloat16)
+        self.do_seq = do.to(self.dev)
+        self.do_shard = torch.empty_like(self.shard[0])
+        S = L // N
+        self.dq = torch.empty((N, B, S, H, d), dtype=torch.float32, device=self.dev)
+        self.dk = torch.empty((N, B, S, self.Hkv, d), dtype=torch.float32, device=self.dev)
+        self.dv = torch.empty_like(self.dk)
+        self.dq_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=self.dev)
+        self.dk_seq = torch.empty((B, L, self.Hkv, d), dtype=torch.float32, device=self.dev)
+        self.dv_seq = torch.empty_like(self.dk_seq)
+        self.bws = ra.new_workspace(ra.ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N), device=self.dev)
+        self.flops = 2.0 * self.flops
+        self.launches = 1 + 3 + 3
+
+    def step_bwd(self, time_attention=False):
+        ra, B, L, H, d, N = self.ra, self.B, self.L, self.H, self.d, self.N
+        ra.ra_shard_permute(self.do_seq, self.do_shard, ra.RA_SEQ_TO_SHARDS, self.layout, B, L, H, d, N)
+        if time_attention:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        ra.ra_ring_attn_bwd(*self.shard, self.o_ring, self.do_shard, self.lse_ring, self.dq, self.dk, self.dv,
+                            B, L, H, self.Hkv, d, N, self.layout, self.causal, workspace=self.bws)
+        if time_attention:
+            e1.record()
+            self.attn_events.append((e0, e1))
+        ra.ra_shard_permute(self.dq, self.dq_seq, ra.RA_SHARDS_TO_SEQ, self.layout, B, L, H, d, N)
+        ra.ra_shard_permute(self.dk, self.dk_seq, ra.RA_SHARDS_TO_SEQ, self.layout, B, L, self.Hkv, d, N)
+        ra.ra_shard_permute(self.dv, self.dv_seq, ra.RA_SHARDS_TO_SEQ, self.layout, B, L, self.Hkv, d, N)
+
     def step_e2e(self):
         for h, s in zip(self.host, self.seq):
             s.copy_(h, non_blocking=True)
@@ -347,6 +384,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--stepwise", action="store_true",
                     help="run the sweep as N block launches + N-1 LSE merges (the pages' per-step loop)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward (ra_ring_attn_bwd) on saved forward outputs instead")
     ap.add_argument("--varlen", type=int, default=None,
                     help="pack this many variable-length sequences (seeded cut points) into the workload")
     ap.add_argument("--kv-heads", type=int, default=None,
@@ -376,36 +415,46 @@ def main():
     wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise, kv_heads=args.kv_heads,
                   varlen=args.varlen)
 
+    step = wl.step
+    if args.backward:
+        wl.prepare_backward()
+        step = wl.step_bwd
     for _ in range(args.warmup):
-        wl.step()
+        step()
     torch.cuda.synchronize()
     ra.ra_check_status(wl.ws)
 
     # device-resident timed region
     wl.attn_events = []
     with ClockSampler(local_rank) as clocks:
-        ms = timed(lambda: wl.step(time_attention=True), args.steps, world, dev)
+        ms = timed(lambda: step(time_attention=True), args.steps, world, dev)
     ms_step = ms / args.steps
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in wl.attn_events]))
     attn_ms = max_over_ranks(attn_ms, world, dev)
     ra.ra_check_status(wl.ws)
 
     # end to end through the same calls, host buffers in and out
-    for _ in range(2):
-        wl.step_e2e()
-    ms_e2e = timed(wl.step_e2e, args.steps, world, dev) / args.steps
-    ra.ra_check_status(wl.ws)
+    if args.backward:
+        ms_e2e = None
+    else:
+        for _ in range(2):
+            wl.step_e2e()
+        ms_e2e = timed(wl.step_e2e, args.steps, world, dev) / args.steps
+        ra.ra_check_status(wl.ws)
 
     value = job_value(wl.flops, world, ms_step)
-    e2e_value = job_value(wl.flops, world, ms_e2e)
+    e2e_value = job_value(wl.flops, world, ms_e2e) if ms_e2e else None
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     achieved = wl.flops / (attn_ms * 1e-3) / 1e12
-    traffic = read_traffic()
+    # the committed DRAM figure is for the default forward launch only
+    default_launch = not (args.backward or args.stepwise or args.varlen or args.kv_heads or shape
+                          or args.workload != DEFAULT_WORKLOAD or layout != "striped")
+    traffic = read_traffic() if default_launch else None
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload + ("" if shape is None else " (resized)"), "layout": layout, "B": wl.B, "L": wl.L, "H": wl.H,
@@ -416,7 +465,8 @@ def main():
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": ("ra_ring_attn_fwd stepwise: N x attn_fwd_kernel<fp32 partial> + N-1 x lse_merge_kernel"
+                     "kernel": ("ra_ring_attn_bwd: bwd_dot + attn_bwd_dkv + attn_bwd_dq" if args.backward else
+                                "ra_ring_attn_fwd stepwise: N x attn_fwd_kernel<fp32 partial> + N-1 x lse_merge_kernel"
                                 if args.stepwise else "attn_fwd_kernel<128, fp32 O> (ra_ring_attn_fwd)"),
                      "kernel_ms": attn_ms,
                      "peak_source": "%s bf16_tflops_sustained" % peak_src},

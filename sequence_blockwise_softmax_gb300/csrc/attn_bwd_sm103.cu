@@ -89,6 +89,25 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint6
     mma_ts_elect<56, 896>(d_tmem, a_tmem, b0, IDESC, 1u);
 }
 
+// The same product in two halves of the 128-long K dimension (HALF 0: rows
+// 0-63 of B / columns 0-31 of A; HALF 1: the rest), so the first half can run
+// while the elementwise warps still produce the second.
+template <int D, int HALF>
+__device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, bool first) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, D, true);
+    if (HALF == 0) {
+        mma_ts_elect<0, 0>(d_tmem, a_tmem, b0, IDESC, first ? 0u : 1u);
+        mma_ts_elect<8, 128>(d_tmem, a_tmem, b0, IDESC, 1u);
+        mma_ts_elect<16, 256>(d_tmem, a_tmem, b0, IDESC, 1u);
+        mma_ts_elect<24, 384>(d_tmem, a_tmem, b0, IDESC, 1u);
+    } else {
+        mma_ts_elect<32, 512>(d_tmem, a_tmem, b0, IDESC, 1u);
+        mma_ts_elect<40, 640>(d_tmem, a_tmem, b0, IDESC, 1u);
+        mma_ts_elect<48, 768>(d_tmem, a_tmem, b0, IDESC, 1u);
+        mma_ts_elect<56, 896>(d_tmem, a_tmem, b0, IDESC, 1u);
+    }
+}
+
 // Write 32 accumulator columns of one row (scaled) as fp32.
 __device__ __forceinline__ void store_row32(float *dst, const uint32_t (&r)[32], float mul) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
@@ -132,8 +151,8 @@ struct BwdQSmem {
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBars = kV + kStages * kTile;
     // Q+dO full, K full[2], V full[2], K empty[2], V empty[2], S full, dP full,
-    // dS full, dQ done, final
-    static constexpr int kNumBars = 1 + 4 * kStages + 5;
+    // dS full (keys 0-63), dS full (keys 64-127), dQ done, final
+    static constexpr int kNumBars = 1 + 4 * kStages + 6;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;
 };
@@ -153,7 +172,7 @@ __global__ void __launch_bounds__(256, 1)
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KEMPTY = 1 + 2 * NS, B_VEMPTY = 1 + 3 * NS,
               B_SFULL = 1 + 4 * NS, B_DPFULL = B_SFULL + 1, B_DSFULL = B_SFULL + 2,
-              B_DQDONE = B_SFULL + 3, B_FINAL = B_SFULL + 4;
+              B_DSFULL2 = B_SFULL + 3, B_DQDONE = B_SFULL + 4, B_FINAL = B_SFULL + 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,6 +218,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_DPFULL), 1);
         mbar_init(BAR(B_DSFULL), 128);
+        mbar_init(BAR(B_DSFULL2), 128);
         mbar_init(BAR(B_DQDONE), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
@@ -288,7 +308,11 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts<D>(tmem + 256, tmem, dk_mn + soff, t == 0);          // dQ += dS K
+            issue_ts_half<D, 0>(tmem + 256, tmem, dk_mn + soff, t == 0);  // dQ += dS K, keys 0-63
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_ts_half<D, 1>(tmem + 256, tmem, dk_mn + soff, false);   // keys 64-127
             tc_commit_elect(BAR(B_DQDONE));
             tc_commit_elect(BAR(B_KEMPTY + st));
             __syncwarp();
@@ -347,10 +371,15 @@ __global__ void __launch_bounds__(256, 1)
                                               p1 * (__uint_as_float(pv[c + 1]) - dval));
                 }
                 tmem_st16(tS + 16 * q, out);
+                if (q == 1) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(B_DSFULL));
+                }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(B_DSFULL));
+            mbar_arrive(BAR(B_DSFULL2));
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
@@ -398,8 +427,9 @@ struct BwdKVSmem {
     static constexpr uint32_t kDO = kQ + kStages * kTile;
     static constexpr uint32_t kVec = kDO + kStages * kTile;       // per stage: lse2[128], D[128]
     static constexpr uint32_t kBars = kVec + kStages * 1024;
-    // K+V full, Q full[2], Q empty[2], S full, dP full, P full, MMA done, final
-    static constexpr int kNumBars = 1 + 2 * kStages + 5;
+    // K+V full, Q full[2], Q empty[2], S full, dP full, P full (queries 0-63),
+    // P full (queries 64-127), MMA done, final
+    static constexpr int kNumBars = 1 + 2 * kStages + 6;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;
 };
@@ -451,7 +481,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS, B_DPFULL = B_SFULL + 1,
-              B_PFULL = B_SFULL + 2, B_MMADONE = B_SFULL + 3, B_FINAL = B_SFULL + 4;
+              B_PFULL = B_SFULL + 2, B_PFULL2 = B_SFULL + 3, B_MMADONE = B_SFULL + 4,
+              B_FINAL = B_SFULL + 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -494,6 +525,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_DPFULL), 1);
         mbar_init(BAR(B_PFULL), 128);
+        mbar_init(BAR(B_PFULL2), 128);
         mbar_init(BAR(B_MMADONE), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
@@ -581,8 +613,13 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts<D>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
-            issue_ts<D>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
+            issue_ts_half<D, 0>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
+            issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_ts_half<D, 1>(tmem + 256, tmem, ddo_mn + soff, false);
+            issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128, dq_mn + soff, false);
             tc_commit_elect(BAR(B_MMADONE));
             tc_commit_elect(BAR(B_QEMPTY + st));
             __syncwarp();
@@ -632,23 +669,31 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld32(tP + 32 * q, pv);
                 tmem_wait_ld();
                 uint32_t outp[16], outs[16];
+                const float2 *lv = reinterpret_cast<const float2 *>(vec + 32 * q);
+                const float2 *dv2 = reinterpret_cast<const float2 *>(vec + 128 + 32 * q);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     const int col = 32 * q + c;
-                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -vec[col]));
-                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -vec[col + 1]));
+                    const float2 l2 = lv[c >> 1], dd = dv2[c >> 1];
+                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -l2.x));
+                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2.y));
                     if (col >= lim || col < lim_lo) p0 = 0.f;
                     if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
                     outp[c >> 1] = pack_bf16x2(p0, p1);
-                    outs[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - vec[128 + col]),
-                                               p1 * (__uint_as_float(pv[c + 1]) - vec[128 + col + 1]));
+                    outs[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - dd.x),
+                                               p1 * (__uint_as_float(pv[c + 1]) - dd.y));
                 }
                 tmem_st16(tS + 16 * q, outp);
                 tmem_st16(tP + 16 * q, outs);
+                if (q == 1) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(B_PFULL));
+                }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(B_PFULL));
+            mbar_arrive(BAR(B_PFULL2));
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
