@@ -43,7 +43,7 @@ DEFAULT_WORKLOAD = "striped_B1_H8_L131072_d128_N16"
 LAUNCHES_PER_STEP = 6          # 3 shard permutes, 1 ring sweep, 1 O un-permute, 1 LSE un-permute
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_striped_128k_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "sequence_blockwise_softmax_gb300", "csrc", f)
-                  for f in ("attn_sm103.cu", "ra_device.cuh")]
+                  for f in ("attn_sm103.cu", "ra_device.cuh", "ra_positions.cuh", "ra_internal.h")]
 
 
 def algorithmic_flops(B, L, H, d, causal):
@@ -321,6 +321,79 @@ class Workload:
         return self.o_host.numel() * 4 + self.lse_host.numel() * 4
 
 
+# ----------------------------------------------------------------- ring balance
+def ring_pair_counts(layout, N, S, causal):
+    """Allowed (query, key) pairs that rank i computes at ring step s, where it meets the
+    key/value shard of rank j = (i - s) mod N: an [N, N] table indexed [i, s].
+
+    Counted from the token positions of each layout ("From Ring Attention to DeepSpeed
+    Ulysses to USP", §3.4 contiguous, §4 striped, §6.1 zigzag): contiguous rank r holds
+    r*S .. r*S+S-1, so an earlier rank's shard is all visible, its own is a triangle and a
+    later one is hidden; striped local token a of rank r sits at a*N + r, so a key shard
+    j <= i gives the triangle c <= a and j > i the strict one c < a; zigzag rank r holds
+    chunks r and 2N-1-r of S/2 tokens, which makes every step half a block, plus the two
+    diagonal chunk triangles' extra S/2 on step 0."""
+    c = np.zeros((N, N), dtype=np.int64)
+    for i in range(N):
+        for s in range(N):
+            j = (i - s) % N
+            if not causal:
+                c[i, s] = S * S
+            elif layout == "contiguous":
+                c[i, s] = S * S if j < i else (S * (S + 1) // 2 if j == i else 0)
+            elif layout == "striped":
+                c[i, s] = S * (S + 1) // 2 if j <= i else S * (S - 1) // 2
+            else:
+                C = S // 2
+                c[i, s] = 2 * C * C + (C if j == i else 0)
+    return c
+
+
+def balance_table(layout, N, S, causal):
+    """The ring's critical path in pairs: with one device per rank a step lasts as long as
+    its busiest rank, so the sweep costs sum_s max_i pairs(i, s) against the ideal total / N."""
+    c = ring_pair_counts(layout, N, S, causal)
+    crit = int(c.max(axis=0).sum())
+    ideal = float(c.sum()) / N
+    return {"pairs_total": int(c.sum()), "pairs_step_max": c.max(axis=0).tolist(),
+            "pairs_critical_path": crit, "pairs_ideal": ideal, "pairs_ratio": crit / ideal}
+
+
+def measure_ring_steps(ra, wl, reps=3):
+    """The per-rank stepwise loop, each rank as if it had the whole GPU: for every rank i
+    and step s, one ra_block_attn_fwd against key/value rank (i - s) mod N plus, from step
+    1 on, one ra_lse_merge into the rank's accumulator, timed with CUDA events.  Returns
+    [N, N] milliseconds indexed [i, s] (median over ``reps`` sweeps)."""
+    N, Bq, Hq, d, L = wl.N, wl.Bq, wl.Hq, wl.d, wl.L
+    S = L // N
+    ring = [t.view(N, Bq, S, t.shape[-2], d) for t in (wl.head if wl.U > 1 else wl.shard)]
+    o_acc = torch.empty((Bq, S, Hq, d), dtype=torch.float32, device=wl.dev)
+    lse_acc = torch.empty((Bq, Hq, S), dtype=torch.float32, device=wl.dev)
+    o_b, lse_b = torch.empty_like(o_acc), torch.empty_like(lse_acc)
+    out = np.zeros((reps, N, N))
+    for rep in range(reps):
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(N)] for _ in range(N)]
+        for i in range(N):
+            for s in range(N):
+                j = (i - s) % N
+                o, lse = (o_acc, lse_acc) if s == 0 else (o_b, lse_b)
+                ev[i][s][0].record()
+                if wl.Hkv == wl.H:
+                    ra.ra_block_attn_fwd(ring[0][i], ring[1][j], ring[2][j], o, lse, Bq, S, Hq, d, N, i, j,
+                                         wl.layout, wl.causal, workspace=wl.ws)
+                else:
+                    ra.ra_block_attn_fwd_gqa(ring[0][i], ring[1][j], ring[2][j], o, lse, Bq, S, Hq,
+                                             wl.Hkv // wl.U, d, N, i, j, wl.layout, wl.causal, workspace=wl.ws)
+                if s:
+                    ra.ra_lse_merge(o_acc, lse_acc, o_b, lse_b, Bq, S, Hq, d)
+                ev[i][s][1].record()
+        torch.cuda.synchronize()
+        out[rep] = [[a.elapsed_time(b) for a, b in row] for row in ev]
+    ra.ra_check_status(wl.ws)
+    return np.median(out, axis=0)
+
+
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
@@ -519,6 +592,21 @@ def main():
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks.summary(),
     }
+
+    if wl.cu is None:
+        bal = balance_table(layout, wl.N, wl.L // wl.N, wl.causal)
+        if args.stepwise:
+            # measured after the timed region: every (rank, step) block + merge on the whole GPU
+            t = measure_ring_steps(ra, wl)
+            step_max = t.max(axis=0)
+            bal.update({
+                "step_ms_max": step_max.tolist(), "step_ms_mean": t.mean(axis=0).tolist(),
+                "critical_path_ms": float(step_max.sum()), "ideal_ms": float(t.sum()) / wl.N,
+                "ms_ratio": float(step_max.sum()) / (float(t.sum()) / wl.N),
+                "per_rank_tflops_critical_path": wl.flops / wl.N / (step_max.sum() * 1e-3) / 1e12,
+                "timing": "each rank's block + merge launched alone on the whole GPU, as if every "
+                          "rank had its own; a step lasts as long as its slowest rank"})
+        line["ring_balance"] = bal
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, dt, n, threads = oracle_sample_run(args.workload, args.cpu_budget)
