@@ -5,7 +5,8 @@
 // ("From Ring Attention to DeepSpeed Ulysses to USP", jsqmd.com/news/734632,
 // §3.1: at step s rank i holds the KV of rank (i - s) mod N) and folds every
 // 128-key tile into the running (m, l, O) state of §3.2, so the partial
-// results never leave the SM.
+// results never leave the SM.  Here m is the reference point of the
+// exponentials, not necessarily the running max (see kSumLo below).
 //
 // Causal masking by position (same article §3.4; "What problem does sequence
 // parallelism solve?", model.playoffer.cn, engineering notes: the ring decides
@@ -24,10 +25,10 @@
 //   warp 2      tensor-memory allocator.
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
 //               query row (the 32x32b tensor-memory load gives a thread its
-//               whole row, so row max and row sum need no shuffles), exp2
-//               with the scale folded into log2(e), P written back to
-//               tensor memory as bf16, O rescaled in place when the row max
-//               grows, and the final normalisation and store.
+//               whole row, so row sums need no shuffles), exp2 with the
+//               scale folded into log2(e), P written back to tensor memory
+//               as bf16, O rescaled in place when the reference point
+//               moves, and the final normalisation and store.
 // Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d); P_g is packed bf16 in the first 64
 // columns of S_g.
@@ -84,10 +85,18 @@ struct AttnSmem {
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
 };
 
-// The softmax reference point of a row moves only when the row max exceeds it
-// by more than this (log2 units), so P stays below 2^8 and O is rescaled
-// rarely; O / l does not depend on the reference point.
-constexpr float kRescaleLog2 = 8.0f;
+// Reference point of the exponentials.  The online softmax of §3.2 subtracts
+// the running row max m only to keep exp() in range: O / l and m + ln l are
+// the same for any reference.  A row therefore starts at reference 0 and
+// computes P = 2^(s*scale*log2e - m) without a row max; the reference moves
+// only when the running denominator would leave [kSumLo, kSumHi] (or is not
+// a number), to max(tile max, m + log2 l), which brings the sum into
+// [1, 129].  With l <= 2^32 no P and no partial sum of P can overflow, and
+// with l >= 2^-32 over at most 2^24 keys the largest term is at least
+// 2^-56, so what ex2 flushes to zero (below 2^-126) is less than 2^-70 of
+// it.  For scores of ordinary size (|s * scale| up to about 20) the
+// reference never moves at all.
+constexpr float kSumLo = 0x1p-32f, kSumHi = 0x1p32f;
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(384, 1)
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tO = tmem + lane_off + 256 + g * D;
         const float sl2 = args.scale_log2;
 
-        float m_ref = -INFINITY;  // running max, already scaled to log2 units
+        float m_ref = 0.f;        // reference point of the exponentials (log2 units)
         float l = 0.f;            // running denominator, relative to m_ref
         float lr = 0.f;           // the same sum over the bf16-rounded P the MMA uses
         int64_t my_start, my_end;
@@ -378,82 +387,99 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (!(ok = warp_wait(BAR(B_SFULL + g), t & 1, abort_flag))) break;
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
-            tmem_wait_ld();
-            float *s = reinterpret_cast<float *>(&sr[0][0]);
             const int lim = khi - w.tile * 128;       // columns [lim_lo, lim) are visible
             const int lim_lo = klo - w.tile * 128;
-            if (lim < 128 || lim_lo > 0) {
+            const bool partial = lim < 128 || lim_lo > 0;
+            uint32_t sr[4][32];
+            auto load_s = [&]() {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= lim || c < lim_lo) s[c] = -INFINITY;
-            }
-            // row max: four independent three-input chains
-            float mA = s[0], mB = s[1], mC = s[2], mD = s[3];
+                for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+                tmem_wait_ld();
+                if (partial) {
+                    float *s = reinterpret_cast<float *>(&sr[0][0]);
 #pragma unroll
-            for (int c = 4; c < 128; c += 8) {
-                mA = max3(mA, s[c], s[c + 1]);
-                mB = max3(mB, s[c + 2], s[c + 3]);
-                mC = max3(mC, s[c + 4], s[c + 5]);
-                mD = max3(mD, s[c + 6], s[c + 7]);
-            }
-            const float m_tile = max3(mA, mB, fmaxf(mC, mD)) * sl2;
-            // Lazy rescale: the reference point moves only when the row max
-            // grows by more than 2^kRescaleLog2, so P stays below 2^8 and O and
-            // l are rescaled rarely.  O / l is the same for any reference point.
-            const bool move = m_tile > m_ref + kRescaleLog2;
-            float alpha = 1.f;
-            if (move) {
-                alpha = ex2(m_ref - m_tile);
-                l *= alpha;
-                lr *= alpha;
-                m_ref = m_tile;
-            }
-            // O holds PV of every earlier tile (S_g of this tile was computed
-            // after it); rescale it when any row of the warp moved its reference
-            if (t > 0 && __any_sync(0xffffffffu, move)) {
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + q * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tmem_st32(tO + q * 32, o);
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim || c < lim_lo) s[c] = -INFINITY;
                 }
-            }
-            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
-            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            // P of each 32-column chunk goes to tensor memory as 16 packed
-            // columns at 16*chunk, over S columns this thread has already read
+            };
+            // P is computed against the current reference point and kept in
+            // registers until the row's denominator has been checked; only
+            // when it would leave [kSumLo, kSumHi] (or is not a number) does the
+            // warp reload S (still intact in tensor memory), move the
+            // reference to max(tile max, reference + log2 l) -- the sum then
+            // lies in [1, 129] -- rescale O, l and lr, and compute P again.
+            uint32_t pr[4][16];
+            float lt, lrt;
+            auto p_pass = [&]() {
+                const float *s = reinterpret_cast<const float *>(&sr[0][0]);
+                const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-m_ref, -m_ref);
+                uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t pr[16];
+                for (int q = 0; q < 4; ++q) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float x0, x1;
-                    f32x2_split(fma_f32x2(f32x2(s[32 * q + c], s[32 * q + c + 1]), sl2x2, negm2), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    lsum[(c >> 1) & 3] = add_f32x2(lsum[(c >> 1) & 3], f32x2(p0, p1));
-                    const uint32_t pk = pack_bf16x2(p0, p1);
-                    pr[c >> 1] = pk;
-                    rs[(c >> 1) & 3] = add_bf16x2_to_f32(rs[(c >> 1) & 3], pk);
+                    for (int c = 0; c < 32; c += 2) {
+                        float x0, x1;
+                        f32x2_split(fma_f32x2(f32x2(s[32 * q + c], s[32 * q + c + 1]), sl2x2, negm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        lsum[(c >> 1) & 3] = add_f32x2(lsum[(c >> 1) & 3], f32x2(p0, p1));
+                        const uint32_t pk = pack_bf16x2(p0, p1);
+                        pr[q][c >> 1] = pk;
+                        rs[(c >> 1) & 3] = add_bf16x2_to_f32(rs[(c >> 1) & 3], pk);
+                    }
                 }
-                tmem_st16(tS + 16 * q, pr);
-            }
-            {
                 float a0, a1, b0, b1, c0, c1, d0, d1;
                 f32x2_split(lsum[0], a0, a1);
                 f32x2_split(lsum[1], b0, b1);
                 f32x2_split(lsum[2], c0, c1);
                 f32x2_split(lsum[3], d0, d1);
-                l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-                lr += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                lt = ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                lrt = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+            };
+            load_s();
+            p_pass();
+            {
+                const float ln = l + lt;
+                const bool bad = !(ln >= kSumLo && ln <= kSumHi);
+                if (__builtin_expect(__any_sync(0xffffffffu, bad), 0)) {
+                    load_s();
+                    const float *s = reinterpret_cast<const float *>(&sr[0][0]);
+                    float mA = s[0], mB = s[1];
+#pragma unroll
+                    for (int c = 2; c < 128; c += 4) {
+                        mA = max3(mA, s[c], s[c + 1]);
+                        mB = max3(mB, s[c + 2], s[c + 3]);
+                    }
+                    float m_new = m_ref;
+                    if (bad) {
+                        const float cand = fmaxf(fmaxf(mA, mB) * sl2, l > 0.f ? m_ref + lg2(l) : -INFINITY);
+                        if (cand != -INFINITY) m_new = cand;
+                    }
+                    const float alpha = ex2(m_ref - m_new);
+                    l *= alpha;
+                    lr *= alpha;
+                    m_ref = m_new;
+                    // O holds PV of every earlier tile (S_g of this tile was
+                    // computed after it); the whole warp takes part in the reload
+                    if (t > 0) {
+#pragma unroll 1
+                        for (int q = 0; q < D / 16; ++q) {
+                            uint32_t o[16];
+                            tmem_ld16(tO + q * 16, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                            tmem_st16(tO + q * 16, o);
+                        }
+                    }
+                    p_pass();
+                }
             }
+            // P goes to tensor memory as 64 packed columns over S's first half
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_st16(tS + 16 * q, pr[q]);
+            l += lt;
+            lr += lrt;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(B_PFULL + g));

@@ -65,6 +65,30 @@ def workload_inputs(name):
     return make_qkv(w["B"], w["L"], w["H"], w["d"], w["seed"], w["k_scale_frac"])
 
 
+def make_extreme_qkv(B, L, H, d, seed, mode):
+    """q, k, v (CPU bf16, [B, L, H, d]) whose scores q.k / sqrt(d) are tens of nats from 0:
+      "large"    -- q and k of make_qkv times 4 (exact in bf16): scores ~ N(0, 16^2) nats;
+      "negative" -- every key near one random direction u_h per head (k = u + 0.5 n) and
+                    every query near -4 u_h (q = -4 (u + 0.1 n)): all scores about -45 nats,
+                    spread by a few nats;
+      "mixed"    -- like "negative", with a random sign per query token, so half the rows
+                    score about +45 nats and half about -45."""
+    if mode == "large":
+        q, k, v, _ = make_qkv(B, L, H, d, seed)
+        return (q.float() * 4).to(torch.bfloat16), (k.float() * 4).to(torch.bfloat16), v
+    g = torch.Generator().manual_seed(int(seed))
+    u = torch.randn((H, d), generator=g)
+    k = u + 0.5 * torch.randn((B, L, H, d), generator=g)
+    q = -4.0 * (u + 0.1 * torch.randn((B, L, H, d), generator=g))
+    if mode == "mixed":
+        sign = torch.randint(0, 2, (B, L, 1, 1), generator=g).float() * 2 - 1
+        q = q * sign
+    elif mode != "negative":
+        raise ValueError(mode)
+    v = torch.randn((B, L, H, d), generator=g)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
 def randn_bf16(shape, seed):
     """One bf16 tensor from N(0, 1) with its own seeded generator."""
     g = torch.Generator().manual_seed(int(seed))
