@@ -13,12 +13,19 @@
 //   pass A       one CTA per 128 keys of one (kv rank, batch, kv head):
 //                S^T = K Q^T and dP^T = V dO^T into tensor memory for each
 //                visible 128-query tile of every query rank and every query
-//                head of the group; one thread per key builds P^T and dS^T
-//                (bf16, back into tensor memory); dV += P^T dO and
-//                dK += dS^T Q accumulate in tensor memory.
+//                head of the group; one thread per key builds P^T from S^T
+//                alone, then dS^T once dP^T is there (bf16, back into tensor
+//                memory); dV += P^T dO and dK += dS^T Q accumulate in tensor
+//                memory.  Pipe order S^T(t), dP^T(t), dV(t), dK(t): P^T(t) is
+//                built while dP^T(t) runs and dS^T(t) while dV(t) runs, and
+//                S^T(t+1) / dP^T(t+1) wait only for dV(t) / dK(t), the
+//                products that read the columns they overwrite.
 //   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
 //                visible key tile in ring order; one thread per query builds
-//                dS; dQ += dS K accumulates in tensor memory.
+//                dS; dQ += dS K accumulates in tensor memory.  S/dS is double
+//                buffered and dP is taken into registers first, so S(t+1) and
+//                dP(t+1) run while dS(t) is built; pipe order S(t+1),
+//                dP(t+1), dQ(t).
 // Masks (causal by position, packed sequences) are the forward's: in every
 // layout positions increase along a rank, so the visible partners of a row in
 // a shard form one interval of local indices.
@@ -144,15 +151,18 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const uint16_t *dout, cons
 // ---------------------------------------------------------------- pass B: dQ
 template <int D>
 struct BwdQSmem {
-    static constexpr int kStages = 2;
+    // K lives until dQ(t) has read it, V only until dP(t) has: three K
+    // stages keep the next K loaded while dQ of the one before runs
+    static constexpr int kKStages = 3, kVStages = 2;
     static constexpr uint32_t kTile = 128u * D * 2u;
     static constexpr uint32_t kBox = 128u * 128u;
     static constexpr uint32_t kQ = 0, kDO = kTile, kK = 2 * kTile;
-    static constexpr uint32_t kV = kK + kStages * kTile;
-    static constexpr uint32_t kBars = kV + kStages * kTile;
-    // Q+dO full, K full[2], V full[2], K empty[2], V empty[2], S full, dP full,
-    // dS full (keys 0-63), dS full (keys 64-127), dQ done, final
-    static constexpr int kNumBars = 1 + 4 * kStages + 6;
+    static constexpr uint32_t kV = kK + kKStages * kTile;
+    static constexpr uint32_t kBars = kV + kVStages * kTile;
+    // Q+dO full, K full[3], K empty[3], V full[2], V empty[2], S full[2] (one
+    // per S buffer), dP full, dP free, dS full (keys 0-63), dS full (keys
+    // 64-127), dS seen by the MMA warp, dQ done, final
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 9;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;
 };
@@ -163,16 +173,19 @@ __global__ void __launch_bounds__(256, 1)
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                        const BwdArgs args) {
     using L = BwdQSmem<D>;
-    constexpr int NS = L::kStages;
+    constexpr int NK = L::kKStages, NV = L::kVStages;
     constexpr int HALVES = D / 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = bwd_align1024(smem_raw);
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KEMPTY = 1 + 2 * NS, B_VEMPTY = 1 + 3 * NS,
-              B_SFULL = 1 + 4 * NS, B_DPFULL = B_SFULL + 1, B_DSFULL = B_SFULL + 2,
-              B_DSFULL2 = B_SFULL + 3, B_DQDONE = B_SFULL + 4, B_FINAL = B_SFULL + 5;
+    const int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + NK, B_VFULL = 1 + 2 * NK, B_VEMPTY = 1 + 2 * NK + NV,
+              B_SFULL = 1 + 2 * NK + 2 * NV, B_DPFULL = B_SFULL + 2, B_DPFREE = B_SFULL + 3,
+              B_DSFULL = B_SFULL + 4, B_DSFULL2 = B_SFULL + 5, B_DSACK = B_SFULL + 6,
+              B_DQDONE = B_SFULL + 7, B_FINAL = B_SFULL + 8;
+    // tensor memory: S/dS double buffer at columns 0 and 384, dP at 128, dQ at 256
+    auto s_col = [](int t) -> uint32_t { return (t & 1) ? 384u : 0u; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,16 +222,21 @@ __global__ void __launch_bounds__(256, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QFULL), 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NK; ++s) {
             mbar_init(BAR(B_KFULL + s), 1);
-            mbar_init(BAR(B_VFULL + s), 1);
             mbar_init(BAR(B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(BAR(B_VFULL + s), 1);
             mbar_init(BAR(B_VEMPTY + s), 1);
         }
         mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_SFULL + 1), 1);
         mbar_init(BAR(B_DPFULL), 1);
+        mbar_init(BAR(B_DPFREE), 128);
         mbar_init(BAR(B_DSFULL), 128);
         mbar_init(BAR(B_DSFULL2), 128);
+        mbar_init(BAR(B_DSACK), 1);
         mbar_init(BAR(B_DQDONE), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
@@ -248,22 +266,22 @@ __global__ void __launch_bounds__(256, 1)
         TileWalk w = walk0;
         w.start_step();
         for (; w.valid(); w.next(), ++t) {
-            const int st = t % NS;
+            const int sk = t % NK, sv = t % NV;
             const int zkv = w.j * args.B + b, y = w.tile * 128;
-            if (t >= NS && !(ok = warp_wait(BAR(B_KEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (t >= NK && !(ok = warp_wait(BAR(B_KEMPTY + sk), ((t / NK) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
+                mbar_arrive_expect_tx(BAR(B_KFULL + sk), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
+                    tma_load_3d(s_base + L::kK + sk * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + sk),
                                 hk * D + 64 * c, y, zkv);
             }
             __syncwarp();
             k_issued = t + 1;
-            if (t >= NS && !(ok = warp_wait(BAR(B_VEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
+            if (t >= NV && !(ok = warp_wait(BAR(B_VEMPTY + sv), ((t / NV) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
+                mbar_arrive_expect_tx(BAR(B_VFULL + sv), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
+                    tma_load_3d(s_base + L::kV + sv * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + sv),
                                 hk * D + 64 * c, y, zkv);
             }
             __syncwarp();
@@ -273,10 +291,10 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) bwd_timeout(args.status, abort_flag);
             volatile int never = 0;
             mbar_wait(BAR(B_QFULL), 0, &never);
-            for (int u = (k_issued > NS ? k_issued - NS : 0); u < k_issued; ++u)
-                mbar_wait(BAR(B_KFULL + u % NS), (u / NS) & 1, &never);
-            for (int u = (v_issued > NS ? v_issued - NS : 0); u < v_issued; ++u)
-                mbar_wait(BAR(B_VFULL + u % NS), (u / NS) & 1, &never);
+            for (int u = (k_issued > NK ? k_issued - NK : 0); u < k_issued; ++u)
+                mbar_wait(BAR(B_KFULL + u % NK), (u / NK) & 1, &never);
+            for (int u = (v_issued > NV ? v_issued - NV : 0); u < v_issued; ++u)
+                mbar_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, &never);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -285,37 +303,61 @@ __global__ void __launch_bounds__(256, 1)
         const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);       // K as K-major operand
         const uint64_t dk_mn = sdesc_sw128(s_base + L::kK, L::kBox, 1024); // K as MN-major operand
         const uint64_t dv_k = sdesc_sw128(s_base + L::kV, 16, 1024);
+        // Pipe order: S(0), dP(0), then per tile t: S(t+1), dP(t+1), dQ(t).
+        // S(t+1) goes to the S buffer dQ(t-1) read dS from, so it waits for
+        // that commit; dP(t+1) overwrites dP(t), so it waits until the
+        // elementwise warps hold dP(t) in registers.
+        auto issue_s = [&](int u) {
+            issue_kmajor<D>(tmem + s_col(u), dq_desc, dk_k + (uint64_t)((u % NK) * (L::kTile >> 4)));
+            tc_commit_elect(BAR(B_SFULL + (u & 1)));
+        };
+        auto issue_dp = [&](int u) {
+            issue_kmajor<D>(tmem + 128, ddo_desc, dv_k + (uint64_t)((u % NV) * (L::kTile >> 4)));
+            tc_commit_elect(BAR(B_DPFULL));
+            tc_commit_elect(BAR(B_VEMPTY + u % NV));
+        };
         bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
         TileWalk w = walk0;
         w.start_step();
         int t = 0;
-        for (; ok && w.valid(); w.next(), ++t) {
-            const int st = t % NS;
-            const uint32_t ph = (t / NS) & 1;
-            const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
-            if (!(ok = warp_wait(BAR(B_KFULL + st), ph, abort_flag))) break;
-            // dS of the previous tile (in the S columns) must be consumed
-            if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE), (t - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_kmajor<D>(tmem, dq_desc, dk_k + soff);                 // S = Q K^T
-            tc_commit_elect(BAR(B_SFULL));
+        if (ok && w.valid()) {
+            ok = warp_wait(BAR(B_KFULL), 0, abort_flag) && warp_wait(BAR(B_VFULL), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
+            }
             __syncwarp();
-            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
-            tc_fence_after();
-            issue_kmajor<D>(tmem + 128, ddo_desc, dv_k + soff);          // dP = dO V^T
-            tc_commit_elect(BAR(B_DPFULL));
-            tc_commit_elect(BAR(B_VEMPTY + st));
-            __syncwarp();
+        }
+        while (ok && w.valid()) {
+            w.next();
+            const bool has_next = w.valid();
+            if (has_next) {
+                const int u = t + 1;
+                if (!(ok = warp_wait(BAR(B_KFULL + u % NK), (u / NK) & 1, abort_flag))) break;
+                if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE), (t - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_s(u);
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_DPFREE), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_dp(u);
+                __syncwarp();
+            }
+            const uint64_t koff = (uint64_t)((t % NK) * (L::kTile >> 4));
             if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts_half<D, 0>(tmem + 256, tmem, dk_mn + soff, t == 0);  // dQ += dS K, keys 0-63
+            issue_ts_half<D, 0>(tmem + 256, tmem + s_col(t), dk_mn + koff, t == 0);  // dQ += dS K, keys 0-63
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
+            if (lane == 0) mbar_arrive(BAR(B_DSACK));     // both halves of dS(t) seen
             tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256, tmem, dk_mn + soff, false);   // keys 64-127
+            issue_ts_half<D, 1>(tmem + 256, tmem + s_col(t), dk_mn + koff, false);   // keys 64-127
             tc_commit_elect(BAR(B_DQDONE));
-            tc_commit_elect(BAR(B_KEMPTY + st));
+            tc_commit_elect(BAR(B_KEMPTY + t % NK));
             __syncwarp();
+            ++t;
         }
         if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
         __syncwarp();
@@ -349,37 +391,56 @@ __global__ void __launch_bounds__(256, 1)
                 klo = (int)keys_upto(args.layout, w.j, lo_pos, N, S);
                 khi = (int)keys_upto(args.layout, w.j, hi_pos, N, S);
             }
-            if (!(ok = warp_wait(BAR(B_SFULL), t & 1, abort_flag))) break;
+            // Tile t starts only once the MMA warp has seen both halves of
+            // dS(t-1).  dP(t) is issued before that, so without this wait the
+            // warps could publish dS(t) before the MMA warp waited for dS(t-1),
+            // or a fast warp could count towards tile t while a slow one is
+            // still on tile t-1: the dS-full barriers count arrivals, not tiles.
+            if (t > 0 && !(ok = warp_wait(BAR(B_DSACK), (t - 1) & 1, abort_flag))) break;
+            // dP(t) into registers first, so the next dP can be computed meanwhile
             if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
             tc_fence_after();
+            uint32_t dpv[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tP + 32 * q, dpv[q]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(BAR(B_DPFREE));
+            if (!(ok = warp_wait(BAR(B_SFULL + (t & 1)), (t >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t tSb = tS + s_col(t);
             const int lim = khi - w.tile * 128, lim_lo = klo - w.tile * 128;
+            const bool partial = lim < 128 || lim_lo > 0;
+            const uint64_t sl2x2 = f32x2(sl2, sl2), nl2 = f32x2(-lse2, -lse2), dd2 = f32x2(dval, dval);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t sv[32], pv[32];
-                tmem_ld32(tS + 32 * q, sv);
-                tmem_ld32(tP + 32 * q, pv);
+                uint32_t sv[32], out[16];
+                tmem_ld32(tSb + 32 * q, sv);
                 tmem_wait_ld();
-                uint32_t out[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const int col = 32 * q + c;
-                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
-                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2));
-                    if (col >= lim || col < lim_lo) p0 = 0.f;
-                    if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
-                    out[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - dval),
-                                              p1 * (__uint_as_float(pv[c + 1]) - dval));
+                    float x0, x1;
+                    f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2),
+                                x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    if (partial) {
+                        const int col = 32 * q + c;
+                        if (col >= lim || col < lim_lo) p0 = 0.f;
+                        if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
+                    }
+                    float d0, d1;
+                    f32x2_split(mul_f32x2(f32x2(p0, p1),
+                                          sub_f32x2(f32x2(__uint_as_float(dpv[q][c]), __uint_as_float(dpv[q][c + 1])),
+                                                    dd2)), d0, d1);
+                    out[c >> 1] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(tS + 16 * q, out);
-                if (q == 1) {
+                tmem_st16(tSb + 16 * q, out);
+                if (q == 1 || q == 3) {
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(BAR(B_DSFULL));
+                    mbar_arrive(BAR(q == 1 ? B_DSFULL : B_DSFULL2));
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR(B_DSFULL2));
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
@@ -428,8 +489,9 @@ struct BwdKVSmem {
     static constexpr uint32_t kVec = kDO + kStages * kTile;       // per stage: lse2[128], D[128]
     static constexpr uint32_t kBars = kVec + kStages * 1024;
     // K+V full, Q full[2], Q empty[2], S full, dP full, P full (queries 0-63),
-    // P full (queries 64-127), MMA done, final
-    static constexpr int kNumBars = 1 + 2 * kStages + 6;
+    // P full (queries 64-127), dS full (0-63), dS full (64-127), dV done,
+    // dK done, final
+    static constexpr int kNumBars = 1 + 2 * kStages + 9;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;
 };
@@ -481,8 +543,9 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS, B_DPFULL = B_SFULL + 1,
-              B_PFULL = B_SFULL + 2, B_PFULL2 = B_SFULL + 3, B_MMADONE = B_SFULL + 4,
-              B_FINAL = B_SFULL + 5;
+              B_PFULL = B_SFULL + 2, B_PFULL2 = B_SFULL + 3, B_DSFULL = B_SFULL + 4,
+              B_DSFULL2 = B_SFULL + 5, B_DVDONE = B_SFULL + 6, B_DKDONE = B_SFULL + 7,
+              B_FINAL = B_SFULL + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -526,7 +589,10 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(BAR(B_DPFULL), 1);
         mbar_init(BAR(B_PFULL), 128);
         mbar_init(BAR(B_PFULL2), 128);
-        mbar_init(BAR(B_MMADONE), 1);
+        mbar_init(BAR(B_DSFULL), 128);
+        mbar_init(BAR(B_DSFULL2), 128);
+        mbar_init(BAR(B_DVDONE), 1);
+        mbar_init(BAR(B_DKDONE), 1);
         mbar_init(BAR(B_FINAL), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -558,6 +624,16 @@ __global__ void __launch_bounds__(256, 1)
             const int st = t % NS;
             const int h = hk * group + w.head;
             const int zq = w.i * args.B + b, y = w.tile * 128;
+            // -lse*log2(e) and D of the 128 query rows (0 past the shard's end),
+            // read before the stage wait so their latency overlaps it
+            const size_t base = ((size_t)zq * H + h) * S;
+            float nl[4], dd[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = y + lane * 4 + e;
+                nl[e] = row < S ? args.lse[base + row] * -1.4426950408889634f : 0.f;
+                dd[e] = row < S ? args.dvec[base + row] : 0.f;
+            }
             if (t >= NS && !(ok = warp_wait(BAR(B_QEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_QFULL + st), 2 * L::kTile);
@@ -568,15 +644,9 @@ __global__ void __launch_bounds__(256, 1)
                                 h * D + 64 * c, y, zq);
                 }
             }
-            // lse2 and D of the 128 query rows (0 past the shard's end)
             float *vec = reinterpret_cast<float *>(smem + L::kVec + st * 1024);
-            const size_t base = ((size_t)zq * H + h) * S;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = y + lane * 4 + e;
-                vec[lane * 4 + e] = row < S ? args.lse[base + row] * 1.4426950408889634f : 0.f;
-                vec[128 + lane * 4 + e] = row < S ? args.dvec[base + row] : 0.f;
-            }
+            *reinterpret_cast<float4 *>(vec + lane * 4) = make_float4(nl[0], nl[1], nl[2], nl[3]);
+            *reinterpret_cast<float4 *>(vec + 128 + lane * 4) = make_float4(dd[0], dd[1], dd[2], dd[3]);
             mbar_arrive(BAR(B_QFULL + st));
             __syncwarp();
             issued = t + 1;
@@ -596,6 +666,10 @@ __global__ void __launch_bounds__(256, 1)
         const uint64_t ddo_k = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dq_mn = sdesc_sw128(s_base + L::kQ, L::kBox, 1024);
         const uint64_t ddo_mn = sdesc_sw128(s_base + L::kDO, L::kBox, 1024);
+        // Pipe order per query tile t: S^T(t), dP^T(t), dV(t), dK(t).  S^T(t)
+        // overwrites the columns dV(t-1) reads P^T from, and dP^T(t) those
+        // dK(t-1) reads dS^T from, so each waits for that product's commit --
+        // which lands while the pipe still runs the other one.
         bool ok = warp_wait(BAR(B_KVFULL), 0, abort_flag);
         QWalk w = walk0;
         w.start();
@@ -604,23 +678,33 @@ __global__ void __launch_bounds__(256, 1)
             const int st = t % NS;
             const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
             if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
-            if (t > 0 && !(ok = warp_wait(BAR(B_MMADONE), (t - 1) & 1, abort_flag))) break;
+            if (t > 0 && !(ok = warp_wait(BAR(B_DVDONE), (t - 1) & 1, abort_flag))) break;
             tc_fence_after();
             issue_kmajor<D>(tmem, dk_k, dq_k + soff);            // S^T = K Q^T
             tc_commit_elect(BAR(B_SFULL));
+            __syncwarp();
+            if (t > 0 && !(ok = warp_wait(BAR(B_DKDONE), (t - 1) & 1, abort_flag))) break;
+            tc_fence_after();
             issue_kmajor<D>(tmem + 128, dv_k, ddo_k + soff);     // dP^T = V dO^T
             tc_commit_elect(BAR(B_DPFULL));
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 0>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
-            issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 1>(tmem + 256, tmem, ddo_mn + soff, false);
+            tc_commit_elect(BAR(B_DVDONE));
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
+            tc_fence_after();
             issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128, dq_mn + soff, false);
-            tc_commit_elect(BAR(B_MMADONE));
+            tc_commit_elect(BAR(B_DKDONE));
             tc_commit_elect(BAR(B_QEMPTY + st));
             __syncwarp();
         }
@@ -655,52 +739,76 @@ __global__ void __launch_bounds__(256, 1)
                 qhi = (int)keys_upto(args.layout, w.i, hi_pos, N, S);
             }
             const int st = t % NS;
+            // phase 1: P^T from S^T alone (the vectors came with the Q stage)
             if (!(ok = warp_wait(BAR(B_SFULL), t & 1, abort_flag))) break;
-            if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
-            // the lse2 / D vectors of this tile (stored before the QFULL arrivals)
             if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
             tc_fence_after();
             const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 1024);
             const int lim = qhi - w.tile * 128, lim_lo = qlo - w.tile * 128;
+            const bool partial = lim < 128 || lim_lo > 0;
+            uint32_t pv[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32 * q, pv[q]);
+            tmem_wait_ld();
+            const uint64_t sl2x2 = f32x2(sl2, sl2);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t sv[32], pv[32];
-                tmem_ld32(tS + 32 * q, sv);
-                tmem_ld32(tP + 32 * q, pv);
-                tmem_wait_ld();
-                uint32_t outp[16], outs[16];
-                const float2 *lv = reinterpret_cast<const float2 *>(vec + 32 * q);
-                const float2 *dv2 = reinterpret_cast<const float2 *>(vec + 128 + 32 * q);
+                uint32_t outp[16];
+                const uint64_t *nl2 = reinterpret_cast<const uint64_t *>(vec + 32 * q);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const int col = 32 * q + c;
-                    const float2 l2 = lv[c >> 1], dd = dv2[c >> 1];
-                    float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -l2.x));
-                    float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2.y));
-                    if (col >= lim || col < lim_lo) p0 = 0.f;
-                    if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
+                    float x0, x1;
+                    f32x2_split(fma_f32x2(f32x2(__uint_as_float(pv[q][c]), __uint_as_float(pv[q][c + 1])),
+                                          sl2x2, nl2[c >> 1]), x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    if (partial) {
+                        const int col = 32 * q + c;
+                        if (col >= lim || col < lim_lo) p0 = 0.f;
+                        if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
+                    }
+                    pv[q][c] = __float_as_uint(p0);
+                    pv[q][c + 1] = __float_as_uint(p1);
                     outp[c >> 1] = pack_bf16x2(p0, p1);
-                    outs[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(pv[c]) - dd.x),
-                                               p1 * (__uint_as_float(pv[c + 1]) - dd.y));
                 }
                 tmem_st16(tS + 16 * q, outp);
-                tmem_st16(tP + 16 * q, outs);
-                if (q == 1) {
+                if (q == 1 || q == 3) {
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(BAR(B_PFULL));
+                    mbar_arrive(BAR(q == 1 ? B_PFULL : B_PFULL2));
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR(B_PFULL2));
+            // phase 2: dS^T = P^T (dP^T - D), 32 columns at a time
+            if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t dp[32], outs[16];
+                tmem_ld32(tP + 32 * q, dp);
+                tmem_wait_ld();
+                const uint64_t *dd2 = reinterpret_cast<const uint64_t *>(vec + 128 + 32 * q);
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float d0, d1;
+                    f32x2_split(mul_f32x2(f32x2(__uint_as_float(pv[q][c]), __uint_as_float(pv[q][c + 1])),
+                                          sub_f32x2(f32x2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                                    dd2[c >> 1])), d0, d1);
+                    outs[c >> 1] = pack_bf16x2(d0, d1);
+                }
+                tmem_st16(tP + 16 * q, outs);
+                if (q == 1 || q == 3) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(q == 1 ? B_DSFULL : B_DSFULL2));
+                }
+            }
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
         } else {
             const int T = t;
             if (T > 0) {
-                ok = warp_wait(BAR(B_MMADONE), (T - 1) & 1, abort_flag);
+                ok = warp_wait(BAR(B_DVDONE), (T - 1) & 1, abort_flag) &&
+                     warp_wait(BAR(B_DKDONE), (T - 1) & 1, abort_flag);
                 if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
                 tc_fence_after();
             }
