@@ -378,7 +378,8 @@ __global__ void __launch_bounds__(256, 1)
         seq_bounds(args.cu_seqlens, args.n_seqs, total, my_pos, my_start, my_end);
         const int64_t lo_pos = my_start - 1, hi_pos = args.causal ? my_pos : my_end - 1;
         const size_t vi = ((size_t)zq * H + h) * S + a_c;
-        const float lse2 = args.lse[vi] * 1.4426950408889634f;
+        const float lse_v = args.lse[vi];
+        const float lse2 = lse_v > -INFINITY ? lse_v * 1.4426950408889634f : 0.f;   // no key: P = 0 anyway
         const float dval = args.dvec[vi];
         const float sl2 = args.scale_log2;
         TileWalk w = walk0;
@@ -417,17 +418,17 @@ __global__ void __launch_bounds__(256, 1)
                 uint32_t sv[32], out[16];
                 tmem_ld32(tSb + 32 * q, sv);
                 tmem_wait_ld();
+                if (partial) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (32 * q + c >= lim || 32 * q + c < lim_lo) sv[c] = __float_as_uint(-INFINITY);
+                }
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float x0, x1;
                     f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2),
                                 x0, x1);
-                    float p0 = ex2(x0), p1 = ex2(x1);
-                    if (partial) {
-                        const int col = 32 * q + c;
-                        if (col >= lim || col < lim_lo) p0 = 0.f;
-                        if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
-                    }
+                    const float p0 = ex2(x0), p1 = ex2(x1);
                     float d0, d1;
                     f32x2_split(mul_f32x2(f32x2(p0, p1),
                                           sub_f32x2(f32x2(__uint_as_float(dpv[q][c]), __uint_as_float(dpv[q][c + 1])),
@@ -631,7 +632,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int row = y + lane * 4 + e;
-                nl[e] = row < S ? args.lse[base + row] * -1.4426950408889634f : 0.f;
+                const float lv = row < S ? args.lse[base + row] : 0.f;
+                nl[e] = lv > -INFINITY ? lv * -1.4426950408889634f : 0.f;
                 dd[e] = row < S ? args.dvec[base + row] : 0.f;
             }
             if (t >= NS && !(ok = warp_wait(BAR(B_QEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
@@ -745,11 +747,19 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
             const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 1024);
             const int lim = qhi - w.tile * 128, lim_lo = qlo - w.tile * 128;
-            const bool partial = lim < 128 || lim_lo > 0;
             uint32_t pv[4][32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32 * q, pv[q]);
             tmem_wait_ld();
+            // masked queries get S = -inf (P = 0) in a loop of their own, so the
+            // exponential loop below stays one block the compiler can schedule
+            if (lim < 128 || lim_lo > 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (32 * q + c >= lim || 32 * q + c < lim_lo) pv[q][c] = __float_as_uint(-INFINITY);
+            }
             const uint64_t sl2x2 = f32x2(sl2, sl2);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -760,12 +770,7 @@ __global__ void __launch_bounds__(256, 1)
                     float x0, x1;
                     f32x2_split(fma_f32x2(f32x2(__uint_as_float(pv[q][c]), __uint_as_float(pv[q][c + 1])),
                                           sl2x2, nl2[c >> 1]), x0, x1);
-                    float p0 = ex2(x0), p1 = ex2(x1);
-                    if (partial) {
-                        const int col = 32 * q + c;
-                        if (col >= lim || col < lim_lo) p0 = 0.f;
-                        if (col + 1 >= lim || col + 1 < lim_lo) p1 = 0.f;
-                    }
+                    const float p0 = ex2(x0), p1 = ex2(x1);
                     pv[q][c] = __float_as_uint(p0);
                     pv[q][c + 1] = __float_as_uint(p1);
                     outp[c >> 1] = pack_bf16x2(p0, p1);
