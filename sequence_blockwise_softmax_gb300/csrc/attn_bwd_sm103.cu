@@ -16,10 +16,11 @@
 //                head of the group; one thread per key builds P^T from S^T
 //                alone, then dS^T once dP^T is there (bf16, back into tensor
 //                memory); dV += P^T dO and dK += dS^T Q accumulate in tensor
-//                memory.  Pipe order S^T(t), dP^T(t), dV(t), dK(t): P^T(t) is
-//                built while dP^T(t) runs and dS^T(t) while dV(t) runs, and
-//                S^T(t+1) / dP^T(t+1) wait only for dV(t) / dK(t), the
-//                products that read the columns they overwrite.
+//                memory.  Pipe order dV(t), half of dK(t), S^T(t+1), the other
+//                half of dK(t), dP^T(t+1): P^T(t+1) is built while dK(t) and
+//                dP^T(t+1) run, dS^T(t+1) while dV(t+1) runs, and S^T(t+1) /
+//                dP^T(t+1) wait only for dV(t) / dK(t), the products that read
+//                the columns they overwrite.
 //   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
 //                visible key tile in ring order; one thread per query builds
 //                dS; dQ += dS K accumulates in tensor memory.  S/dS is double
@@ -30,9 +31,11 @@
 // layout positions increase along a rank, so the visible partners of a row in
 // a shard form one interval of local indices.
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer
-// (elect.sync), warp 2 tensor-memory allocator, warps 4-7 the elementwise
-// warpgroup (thread = tensor-memory lane).  Every wait is bounded.
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer
+// (elect.sync), warp 2 tensor-memory allocator, warps 4-11 the elementwise
+// threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
+// a tile and warps 8-11 the last 64 (no product here reduces along a row, so
+// the halves never exchange data).  Every wait is bounded.
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -168,7 +171,7 @@ struct BwdQSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                        const BwdArgs args) {
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_SFULL + 1), 1);
         mbar_init(BAR(B_DPFULL), 1);
-        mbar_init(BAR(B_DPFREE), 128);
+        mbar_init(BAR(B_DPFREE), 256);
         mbar_init(BAR(B_DSFULL), 128);
         mbar_init(BAR(B_DSFULL2), 128);
         mbar_init(BAR(B_DSACK), 1);
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(256, 1)
             if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
             if (lane == 0) mbar_arrive(BAR(B_DSACK));     // both halves of dS(t) seen
             tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256, tmem + s_col(t), dk_mn + koff, false);   // keys 64-127
+            issue_ts_half<D, 1>(tmem + 256, tmem + s_col(t) + 32, dk_mn + koff, false);   // keys 64-127
             tc_commit_elect(BAR(B_DQDONE));
             tc_commit_elect(BAR(B_KEMPTY + t % NK));
             __syncwarp();
@@ -366,8 +369,12 @@ __global__ void __launch_bounds__(256, 1)
         volatile int never = 0;
         mbar_wait(BAR(B_FINAL), 0, &never);
     } else if (warp >= 4) {
-        // ------------------------------------------------ dS, one thread per query row
+        // ------------------------------------------------ dS, two threads per query row:
+        // warps 4-7 take keys 0-63, warps 8-11 keys 64-127 (dS has no row
+        // reduction, so the halves never talk).  Each half writes its packed dS
+        // over its own S columns: keys 0-63 at 0-31, keys 64-127 at 64-95.
         const int wq = warp & 3;
+        const int hh = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
         const int a = row0 + r;
         const int a_c = a < S ? a : S - 1;
@@ -398,12 +405,13 @@ __global__ void __launch_bounds__(256, 1)
             // or a fast warp could count towards tile t while a slow one is
             // still on tile t-1: the dS-full barriers count arrivals, not tiles.
             if (t > 0 && !(ok = warp_wait(BAR(B_DSACK), (t - 1) & 1, abort_flag))) break;
-            // dP(t) into registers first, so the next dP can be computed meanwhile
+            // this half's dP(t) into registers first, so the next dP can be
+            // computed meanwhile
             if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
             tc_fence_after();
-            uint32_t dpv[4][32];
+            uint32_t dpv[2][32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tP + 32 * q, dpv[q]);
+            for (int j = 0; j < 2; ++j) tmem_ld32(tP + 64 * hh + 32 * j, dpv[j]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(BAR(B_DPFREE));
@@ -414,14 +422,15 @@ __global__ void __launch_bounds__(256, 1)
             const bool partial = lim < 128 || lim_lo > 0;
             const uint64_t sl2x2 = f32x2(sl2, sl2), nl2 = f32x2(-lse2, -lse2), dd2 = f32x2(dval, dval);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int j = 0; j < 2; ++j) {
+                const int c0 = 64 * hh + 32 * j;      // first key column of this chunk
                 uint32_t sv[32], out[16];
-                tmem_ld32(tSb + 32 * q, sv);
+                tmem_ld32(tSb + c0, sv);
                 tmem_wait_ld();
                 if (partial) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        if (32 * q + c >= lim || 32 * q + c < lim_lo) sv[c] = __float_as_uint(-INFINITY);
+                        if (c0 + c >= lim || c0 + c < lim_lo) sv[c] = __float_as_uint(-INFINITY);
                 }
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
@@ -431,17 +440,15 @@ __global__ void __launch_bounds__(256, 1)
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     float d0, d1;
                     f32x2_split(mul_f32x2(f32x2(p0, p1),
-                                          sub_f32x2(f32x2(__uint_as_float(dpv[q][c]), __uint_as_float(dpv[q][c + 1])),
+                                          sub_f32x2(f32x2(__uint_as_float(dpv[j][c]), __uint_as_float(dpv[j][c + 1])),
                                                     dd2)), d0, d1);
                     out[c >> 1] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(tSb + 16 * q, out);
-                if (q == 1 || q == 3) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(BAR(q == 1 ? B_DSFULL : B_DSFULL2));
-                }
+                tmem_st16(tSb + 64 * hh + 16 * j, out);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(hh == 0 ? B_DSFULL : B_DSFULL2));
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
@@ -452,11 +459,12 @@ __global__ void __launch_bounds__(256, 1)
                 if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
                 tc_fence_after();
             }
-            // tensor-memory loads are warp-wide; only the stores depend on the row
+            // tensor-memory loads are warp-wide; only the stores depend on the row.
+            // Each half writes half of the d columns.
             if (ok) {
                 float *dst = args.dq + (((size_t)zq * S + a_c) * H + h) * D;
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = hh * (D / 64); q < (hh + 1) * (D / 64); ++q) {
                     uint32_t v[32];
                     if (T > 0) {
                         tmem_ld32(tQ + 32 * q, v);
@@ -531,7 +539,7 @@ struct QWalk {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                         const BwdArgs args) {
@@ -668,47 +676,73 @@ __global__ void __launch_bounds__(256, 1)
         const uint64_t ddo_k = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dq_mn = sdesc_sw128(s_base + L::kQ, L::kBox, 1024);
         const uint64_t ddo_mn = sdesc_sw128(s_base + L::kDO, L::kBox, 1024);
-        // Pipe order per query tile t: S^T(t), dP^T(t), dV(t), dK(t).  S^T(t)
-        // overwrites the columns dV(t-1) reads P^T from, and dP^T(t) those
-        // dK(t-1) reads dS^T from, so each waits for that product's commit --
-        // which lands while the pipe still runs the other one.
+        // Pipe order: S^T(0), dP^T(0), then per query tile t: dV(t), the first
+        // half of dK(t), S^T(t+1), the second half of dK(t), dP^T(t+1).  S^T(t+1)
+        // overwrites the columns dV(t) read P^T from and dP^T(t+1) those dK(t)
+        // read dS^T from, so each waits for that product's commit; the first
+        // wait lands while the pipe runs half of dK(t).  S^T(t+1) comes before
+        // the end of dK(t) so that P^T(t+1) is built while dK(t) and dP^T(t+1)
+        // run.
+        auto issue_sT = [&](int u) {
+            issue_kmajor<D>(tmem, dk_k, dq_k + (uint64_t)((u % NS) * (L::kTile >> 4)));   // S^T = K Q^T
+            tc_commit_elect(BAR(B_SFULL));
+        };
+        auto issue_dpT = [&](int u) {
+            issue_kmajor<D>(tmem + 128, dv_k, ddo_k + (uint64_t)((u % NS) * (L::kTile >> 4)));  // dP^T = V dO^T
+            tc_commit_elect(BAR(B_DPFULL));
+        };
         bool ok = warp_wait(BAR(B_KVFULL), 0, abort_flag);
         QWalk w = walk0;
         w.start();
         int t = 0;
-        for (; ok && w.valid(); w.next(), ++t) {
+        if (ok && w.valid()) {
+            ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_sT(0);
+                issue_dpT(0);
+            }
+            __syncwarp();
+        }
+        while (ok && w.valid()) {
             const int st = t % NS;
             const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
-            if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
-            if (t > 0 && !(ok = warp_wait(BAR(B_DVDONE), (t - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_kmajor<D>(tmem, dk_k, dq_k + soff);            // S^T = K Q^T
-            tc_commit_elect(BAR(B_SFULL));
-            __syncwarp();
-            if (t > 0 && !(ok = warp_wait(BAR(B_DKDONE), (t - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_kmajor<D>(tmem + 128, dv_k, ddo_k + soff);     // dP^T = V dO^T
-            tc_commit_elect(BAR(B_DPFULL));
-            __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 0>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256, tmem, ddo_mn + soff, false);
+            issue_ts_half<D, 1>(tmem + 256, tmem + 32, ddo_mn + soff, false);
             tc_commit_elect(BAR(B_DVDONE));
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
             __syncwarp();
+            w.next();
+            const bool has_next = w.valid();
+            const int u = t + 1;
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_DVDONE), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_sT(u);
+                __syncwarp();
+            }
             if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128, dq_mn + soff, false);
+            issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128 + 32, dq_mn + soff, false);
             tc_commit_elect(BAR(B_DKDONE));
             tc_commit_elect(BAR(B_QEMPTY + st));
             __syncwarp();
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_DKDONE), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_dpT(u);
+                __syncwarp();
+            }
+            ++t;
         }
         if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
         __syncwarp();
@@ -717,8 +751,13 @@ __global__ void __launch_bounds__(256, 1)
         volatile int never = 0;
         mbar_wait(BAR(B_FINAL), 0, &never);
     } else if (warp >= 4) {
-        // ------------------------------------------------ P^T, dS^T, one thread per key
+        // ------------------------------------------------ P^T, dS^T, two threads per key:
+        // warps 4-7 take queries 0-63, warps 8-11 queries 64-127 (neither P^T nor
+        // dS^T has a row reduction, so the halves never talk).  Each half writes
+        // its packed result over its own columns: queries 0-63 at 0-31,
+        // queries 64-127 at 64-95.
         const int wq = warp & 3;
+        const int hh = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
         const int kk = c0 + r;
         const int kk_c = kk < S ? kk : S - 1;
@@ -747,65 +786,64 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
             const float *vec = reinterpret_cast<const float *>(smem + L::kVec + st * 1024);
             const int lim = qhi - w.tile * 128, lim_lo = qlo - w.tile * 128;
-            uint32_t pv[4][32];
+            uint32_t pv[2][32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32 * q, pv[q]);
+            for (int j = 0; j < 2; ++j) tmem_ld32(tS + 64 * hh + 32 * j, pv[j]);
             tmem_wait_ld();
             // masked queries get S = -inf (P = 0) in a loop of their own, so the
             // exponential loop below stays one block the compiler can schedule
             if (lim < 128 || lim_lo > 0) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (32 * q + c >= lim || 32 * q + c < lim_lo) pv[q][c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 32; ++c) {
+                        const int col = 64 * hh + 32 * j + c;
+                        if (col >= lim || col < lim_lo) pv[j][c] = __float_as_uint(-INFINITY);
+                    }
             }
             const uint64_t sl2x2 = f32x2(sl2, sl2);
+            // P^T stays in registers only as the packed bf16 the dV product uses
+            uint32_t pk[2][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t outp[16];
-                const uint64_t *nl2 = reinterpret_cast<const uint64_t *>(vec + 32 * q);
+            for (int j = 0; j < 2; ++j) {
+                const uint64_t *nl2 = reinterpret_cast<const uint64_t *>(vec + 64 * hh + 32 * j);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float x0, x1;
-                    f32x2_split(fma_f32x2(f32x2(__uint_as_float(pv[q][c]), __uint_as_float(pv[q][c + 1])),
+                    f32x2_split(fma_f32x2(f32x2(__uint_as_float(pv[j][c]), __uint_as_float(pv[j][c + 1])),
                                           sl2x2, nl2[c >> 1]), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    pv[q][c] = __float_as_uint(p0);
-                    pv[q][c + 1] = __float_as_uint(p1);
-                    outp[c >> 1] = pack_bf16x2(p0, p1);
+                    pk[j][c >> 1] = pack_bf16x2(ex2(x0), ex2(x1));
                 }
-                tmem_st16(tS + 16 * q, outp);
-                if (q == 1 || q == 3) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(BAR(q == 1 ? B_PFULL : B_PFULL2));
-                }
+                tmem_st16(tS + 64 * hh + 16 * j, pk[j]);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(hh == 0 ? B_PFULL : B_PFULL2));
             // phase 2: dS^T = P^T (dP^T - D), 32 columns at a time
             if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t dp[32], outs[16];
-                tmem_ld32(tP + 32 * q, dp);
+                tmem_ld32(tP + 64 * hh + 32 * j, dp);
                 tmem_wait_ld();
-                const uint64_t *dd2 = reinterpret_cast<const uint64_t *>(vec + 128 + 32 * q);
+                const uint64_t *dd2 = reinterpret_cast<const uint64_t *>(vec + 128 + 64 * hh + 32 * j);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
+                    // the rounded P the dV product used: bf16 halves widened exactly
+                    const uint32_t w = pk[j][c >> 1];
+                    const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xffff0000u);
                     float d0, d1;
-                    f32x2_split(mul_f32x2(f32x2(__uint_as_float(pv[q][c]), __uint_as_float(pv[q][c + 1])),
+                    f32x2_split(mul_f32x2(f32x2(p0, p1),
                                           sub_f32x2(f32x2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
                                                     dd2[c >> 1])), d0, d1);
                     outs[c >> 1] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(tP + 16 * q, outs);
-                if (q == 1 || q == 3) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(BAR(q == 1 ? B_DSFULL : B_DSFULL2));
-                }
+                tmem_st16(tP + 64 * hh + 16 * j, outs);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(hh == 0 ? B_DSFULL : B_DSFULL2));
         }
         if (!ok) {
             if (lane == 0) bwd_timeout(args.status, abort_flag);
@@ -817,11 +855,12 @@ __global__ void __launch_bounds__(256, 1)
                 if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
                 tc_fence_after();
             }
-            // tensor-memory loads are warp-wide; only the stores depend on the row
+            // tensor-memory loads are warp-wide; only the stores depend on the row.
+            // Each half writes half of the d columns.
             if (ok) {
                 const size_t row = (((size_t)zk * S + kk_c) * Hkv + hk) * D;
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = hh * (D / 64); q < (hh + 1) * (D / 64); ++q) {
                     uint32_t v[32];
                     if (T > 0) {
                         tmem_ld32(tV + 32 * q, v);
@@ -914,8 +953,8 @@ static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t str
         *err = "too many tiles for one launch";
         return RA_ERR_UNSUPPORTED;
     }
-    kkv<<<(unsigned)grid_kv, 256, BwdKVSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
-    kq<<<(unsigned)grid_q, 256, BwdQSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
+    kkv<<<(unsigned)grid_kv, 384, BwdKVSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
+    kq<<<(unsigned)grid_q, 384, BwdQSmem<D>::kBytes, stream>>>(mq, mk, mv, mdo, args);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *err = cudaGetErrorString(e);
