@@ -264,7 +264,9 @@ RA_API size_t ra_ring_attn_bwd_workspace_bytes(int64_t B, int64_t L, int64_t H, 
 /*
  * ra_check_status -- synchronise `stream`, read the status word at the start
  * of `workspace`, clear it, and return RA_ERR_TIMEOUT if a kernel recorded a
- * timeout since the last check (RA_OK otherwise).
+ * timeout since the last check, RA_ERR_ALIGNMENT if a kernel found its
+ * dynamic shared memory base not 1024-byte aligned (it then computed
+ * nothing), RA_OK otherwise.
  */
 RA_API ra_status ra_check_status(void *workspace, void *stream);
 

@@ -399,6 +399,8 @@ ra_status ra_check_status(void *workspace, void *stream) {
             return fail(RA_ERR_CUDA, "clearing the status word failed");
         if (word & ra::RA_DEV_TIMEOUT_BIT)
             return fail(RA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (status word set)");
+        if (word & ra::RA_DEV_SMEM_ALIGN_BIT)
+            return fail(RA_ERR_ALIGNMENT, "a kernel found its dynamic shared memory base not 1024-byte aligned");
     }
     return RA_OK;
 }

@@ -13,14 +13,14 @@
 //   pass A       one CTA per 128 keys of one (kv rank, batch, kv head):
 //                S^T = K Q^T and dP^T = V dO^T into tensor memory for each
 //                visible 128-query tile of every query rank and every query
-//                head of the group; one thread per key builds P^T from S^T
-//                alone, then dS^T once dP^T is there (bf16, back into tensor
-//                memory); dV += P^T dO and dK += dS^T Q accumulate in tensor
-//                memory.  Pipe order dV(t), half of dK(t), S^T(t+1), the other
-//                half of dK(t), dP^T(t+1): P^T(t+1) is built while dK(t) and
-//                dP^T(t+1) run, dS^T(t+1) while dV(t+1) runs, and S^T(t+1) /
-//                dP^T(t+1) wait only for dV(t) / dK(t), the products that read
-//                the columns they overwrite.
+//                head of the group; the elementwise threads build P^T from
+//                S^T alone (bf16, into shared memory) and then dS^T once dP^T
+//                is there (bf16, back into tensor memory); dV += P^T dO and
+//                dK += dS^T Q accumulate in tensor memory.  Pipe order S^T(t+1),
+//                dV(t), dK(t), dP^T(t+1): with P^T in shared memory, S^T(t+1)
+//                only waits until S^T(t) is in registers, so P^T(t+1) can start
+//                as soon as dS^T(t) is done; dP^T(t+1) waits for dK(t), which
+//                reads the columns it overwrites.
 //   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
 //                visible key tile in ring order; one thread per query builds
 //                dS; dQ += dS K accumulates in tensor memory.  S/dS is double
@@ -115,6 +115,26 @@ __device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, 
         mma_ts_elect<40, 640>(d_tmem, a_tmem, b0, IDESC, 1u);
         mma_ts_elect<48, 768>(d_tmem, a_tmem, b0, IDESC, 1u);
         mma_ts_elect<56, 896>(d_tmem, a_tmem, b0, IDESC, 1u);
+    }
+}
+
+// The same accumulating product with A in shared memory: a 128 x 128 bf16
+// K-major tile stored as two 64-column boxes (HALF 0: columns 0-63, the first
+// box; HALF 1: the second), B as in issue_ts_half.
+template <int D, int HALF>
+__device__ __forceinline__ void issue_ss_half(uint32_t d_tmem, uint64_t a0, uint64_t b0, bool first) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, D, true);
+    constexpr uint32_t hb = (128u * 128u) >> 4;
+    if (HALF == 0) {
+        mma_ss_elect<0, 0>(d_tmem, a0, b0, IDESC, first ? 0u : 1u);
+        mma_ss_elect<2, 128>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<4, 256>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<6, 384>(d_tmem, a0, b0, IDESC, 1u);
+    } else {
+        mma_ss_elect<hb, 512>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<hb + 2, 640>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<hb + 4, 768>(d_tmem, a0, b0, IDESC, 1u);
+        mma_ss_elect<hb + 6, 896>(d_tmem, a0, b0, IDESC, 1u);
     }
 }
 
@@ -495,14 +515,17 @@ struct BwdKVSmem {
     static constexpr uint32_t kK = 0, kV = kTile;
     static constexpr uint32_t kQ = 2 * kTile;
     static constexpr uint32_t kDO = kQ + kStages * kTile;
-    static constexpr uint32_t kVec = kDO + kStages * kTile;       // per stage: lse2[128], D[128]
+    static constexpr uint32_t kP = kDO + kStages * kTile;         // P^T: 128 keys x 128 queries bf16, two boxes
+    static constexpr uint32_t kVec = kP + 2 * kBox;               // per stage: -lse*log2 e [128], D[128]
     static constexpr uint32_t kBars = kVec + kStages * 1024;
-    // K+V full, Q full[2], Q empty[2], S full, dP full, P full (queries 0-63),
-    // P full (queries 64-127), dS full (0-63), dS full (64-127), dV done,
-    // dK done, final
-    static constexpr int kNumBars = 1 + 2 * kStages + 9;
+    // K+V full, Q full[2], Q empty[2], S full, S free, dP full, P full
+    // (queries 0-63), P full (queries 64-127), dS full (0-63), dS full
+    // (64-127), dV done, dK done, final
+    static constexpr int kNumBars = 1 + 2 * kStages + 10;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
-    static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+    // no alignment slack: the kernel requires (and checks) a 1024-byte-aligned
+    // dynamic base, which is what leaves room for P^T
+    static constexpr uint32_t kBytes = kMisc + 16;
 };
 
 // The query tiles a block of keys meets, for each query head of its group and
@@ -546,15 +569,19 @@ __global__ void __launch_bounds__(384, 1)
     using L = BwdKVSmem<D>;
     constexpr int NS = L::kStages;
     constexpr int HALVES = D / 64;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = bwd_align1024(smem_raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if ((smem_u32(smem) & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicOr(args.status, RA_DEV_SMEM_ALIGN_BIT);
+        return;
+    }
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-    const int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS, B_DPFULL = B_SFULL + 1,
-              B_PFULL = B_SFULL + 2, B_PFULL2 = B_SFULL + 3, B_DSFULL = B_SFULL + 4,
-              B_DSFULL2 = B_SFULL + 5, B_DVDONE = B_SFULL + 6, B_DKDONE = B_SFULL + 7,
-              B_FINAL = B_SFULL + 8;
+    const int B_KVFULL = 0, B_QFULL = 1, B_QEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS, B_SFREE = B_SFULL + 1,
+              B_DPFULL = B_SFULL + 2, B_PFULL = B_SFULL + 3, B_PFULL2 = B_SFULL + 4, B_DSFULL = B_SFULL + 5,
+              B_DSFULL2 = B_SFULL + 6, B_DVDONE = B_SFULL + 7, B_DKDONE = B_SFULL + 8,
+              B_FINAL = B_SFULL + 9;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -595,6 +622,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(BAR(B_QEMPTY + s), 1);
         }
         mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_SFREE), 256);
         mbar_init(BAR(B_DPFULL), 1);
         mbar_init(BAR(B_PFULL), 128);
         mbar_init(BAR(B_PFULL2), 128);
@@ -676,13 +704,11 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t ddo_k = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dq_mn = sdesc_sw128(s_base + L::kQ, L::kBox, 1024);
         const uint64_t ddo_mn = sdesc_sw128(s_base + L::kDO, L::kBox, 1024);
-        // Pipe order: S^T(0), dP^T(0), then per query tile t: dV(t), the first
-        // half of dK(t), S^T(t+1), the second half of dK(t), dP^T(t+1).  S^T(t+1)
-        // overwrites the columns dV(t) read P^T from and dP^T(t+1) those dK(t)
-        // read dS^T from, so each waits for that product's commit; the first
-        // wait lands while the pipe runs half of dK(t).  S^T(t+1) comes before
-        // the end of dK(t) so that P^T(t+1) is built while dK(t) and dP^T(t+1)
-        // run.
+        // Pipe order: S^T(0), dP^T(0), then per query tile t: S^T(t+1), dV(t),
+        // dK(t), dP^T(t+1).  P^T lives in shared memory, so S^T(t+1) only waits
+        // until the elementwise threads hold S^T(t) in registers (S free); the
+        // whole of P(t) is built while S^T(t+1) runs.  dP^T(t+1) overwrites the
+        // columns dK(t) reads dS^T from, so it waits for dK(t)'s commit.
         auto issue_sT = [&](int u) {
             issue_kmajor<D>(tmem, dk_k, dq_k + (uint64_t)((u % NS) * (L::kTile >> 4)));   // S^T = K Q^T
             tc_commit_elect(BAR(B_SFULL));
@@ -691,6 +717,7 @@ __global__ void __launch_bounds__(384, 1)
             issue_kmajor<D>(tmem + 128, dv_k, ddo_k + (uint64_t)((u % NS) * (L::kTile >> 4)));  // dP^T = V dO^T
             tc_commit_elect(BAR(B_DPFULL));
         };
+        const uint64_t dp_k = sdesc_sw128(s_base + L::kP, 16, 1024);   // P^T as a K-major operand
         bool ok = warp_wait(BAR(B_KVFULL), 0, abort_flag);
         QWalk w = walk0;
         w.start();
@@ -707,29 +734,29 @@ __global__ void __launch_bounds__(384, 1)
         while (ok && w.valid()) {
             const int st = t % NS;
             const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
+            w.next();
+            const bool has_next = w.valid();
+            const int u = t + 1;
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_SFREE), t & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_sT(u);
+                __syncwarp();
+            }
             if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts_half<D, 0>(tmem + 256, tmem, ddo_mn + soff, t == 0);          // dV += P^T dO
+            issue_ss_half<D, 0>(tmem + 256, dp_k, ddo_mn + soff, t == 0);          // dV += P^T dO
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256, tmem + 32, ddo_mn + soff, false);
+            issue_ss_half<D, 1>(tmem + 256, dp_k, ddo_mn + soff, false);
             tc_commit_elect(BAR(B_DVDONE));
             __syncwarp();
             if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
             __syncwarp();
-            w.next();
-            const bool has_next = w.valid();
-            const int u = t + 1;
-            if (has_next) {
-                if (!(ok = warp_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, abort_flag))) break;
-                if (!(ok = warp_wait(BAR(B_DVDONE), t & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_sT(u);
-                __syncwarp();
-            }
             if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
             tc_fence_after();
             issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128 + 32, dq_mn + soff, false);
@@ -790,6 +817,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int j = 0; j < 2; ++j) tmem_ld32(tS + 64 * hh + 32 * j, pv[j]);
             tmem_wait_ld();
+            // S^T(t) is in registers: the next S^T may overwrite its columns
+            tc_fence_before();
+            mbar_arrive(BAR(B_SFREE));
             // masked queries get S = -inf (P = 0) in a loop of their own, so the
             // exponential loop below stays one block the compiler can schedule
             if (lim < 128 || lim_lo > 0) {
@@ -814,10 +844,20 @@ __global__ void __launch_bounds__(384, 1)
                                           sl2x2, nl2[c >> 1]), x0, x1);
                     pk[j][c >> 1] = pack_bf16x2(ex2(x0), ex2(x1));
                 }
-                tmem_st16(tS + 64 * hh + 16 * j, pk[j]);
             }
-            tmem_wait_st();
-            tc_fence_before();
+            // P^T(t) goes to shared memory (the K-major A operand of dV, in the
+            // 128-byte-swizzled layout a TMA box load would give: 16-byte chunk
+            // j of row r at chunk j ^ (r mod 8)) once dV(t-1) has read P^T(t-1)
+            if (t > 0 && !(ok = warp_wait(BAR(B_DVDONE), (t - 1) & 1, abort_flag))) break;
+            {
+                uint8_t *prow = smem + L::kP + hh * L::kBox + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    *reinterpret_cast<uint4 *>(prow + ((jj ^ (r & 7)) << 4)) =
+                        make_uint4(pk[jj >> 2][(jj & 3) * 4], pk[jj >> 2][(jj & 3) * 4 + 1],
+                                   pk[jj >> 2][(jj & 3) * 4 + 2], pk[jj >> 2][(jj & 3) * 4 + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(BAR(hh == 0 ? B_PFULL : B_PFULL2));
             // phase 2: dS^T = P^T (dP^T - D), 32 columns at a time
             if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;

@@ -10,6 +10,9 @@ namespace ra {
 
 // Bits of the device status word (first 4 bytes of every workspace).
 constexpr unsigned RA_DEV_TIMEOUT_BIT = 1u;
+// A kernel that lays out its shared memory from a 1024-byte-aligned dynamic
+// base found the base unaligned, and returned before touching it.
+constexpr unsigned RA_DEV_SMEM_ALIGN_BIT = 2u;
 
 // One attention launch: every query unit of `num_q_ranks` ranks sweeps its
 // key/value shards.  Ring mode: q/k/v are [N, B, S, H, d] stacks, each query
