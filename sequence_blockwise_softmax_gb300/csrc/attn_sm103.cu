@@ -18,20 +18,22 @@
 // prefix (diagonal tiles are masked in-tile).
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles into a
-//               two-stage ring of shared-memory buffers.
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into one ring
+//               of three shared-memory slots, K a tile ahead of V.
 //   warp 1      MMA issuer (one elected lane): S_g = Q_g K^T into tensor
-//               memory, then O_g += P_g V with P_g read from tensor memory.
+//               memory, then O_g += P_g V with P_g read from shared memory.
 //   warp 2      tensor-memory allocator.
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
 //               query row (the 32x32b tensor-memory load gives a thread its
 //               whole row, so row sums need no shuffles), exp2 with the
-//               scale folded into log2(e), P written back to tensor memory
-//               as bf16, O rescaled in place when the reference point
-//               moves, and the final normalisation and store.
+//               scale folded into log2(e), P written to shared memory as
+//               bf16, O rescaled in place when the reference point moves,
+//               and the final normalisation and store.
 // Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
-// O_0 [256, 256+d), O_1 [256+d, 256+2d); P_g is packed bf16 in the first 64
-// columns of S_g.
+// O_0 [256, 256+d), O_1 [256+d, 256+2d).  Because P does not live in S's
+// columns, S_g(t+1) may be computed while PV_g(t) still runs: the softmax
+// releases S_g as soon as it has read it, and each tile's critical chain is
+// S -> softmax -> PV with no wait on the previous PV in between.
 #include <cmath>
 #include <cstdio>
 
@@ -60,10 +62,6 @@ struct AttnArgs {
     int n_seqs;
 };
 
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __device__ __forceinline__ void record_timeout(unsigned *status, volatile int *abort) {
     *abort = 1;
     atomicOr(status, RA_DEV_TIMEOUT_BIT);
@@ -71,18 +69,20 @@ __device__ __forceinline__ void record_timeout(unsigned *status, volatile int *a
 
 template <int D>
 struct AttnSmem {
-    static constexpr int kStages = 2;
+    static constexpr int kSlots = 3;                     // K/V tile ring
     static constexpr uint32_t kTile = 128u * D * 2u;     // 128 rows x d bf16
     static constexpr uint32_t kBox = 128u * 128u;        // 128 rows x 64 columns
     static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = 2 * kTile;
-    static constexpr uint32_t kV = kK + kStages * kTile;
-    static constexpr uint32_t kBars = kV + kStages * kTile;
-    // barriers: Q full, K full[2], V full[2], K empty[2], V empty[2], S full[2],
+    static constexpr uint32_t kRing = 2 * kTile;
+    static constexpr uint32_t kP = kRing + kSlots * kTile;   // P_g: 128 rows x 128 keys bf16, two boxes each
+    static constexpr uint32_t kBars = kP + 2 * 2 * kBox;
+    // barriers: Q full, slot full[3], slot empty[3], S full[2], S free[2],
     // P full[2], PV done[2], final
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
-    static constexpr uint32_t kBytes = kMisc + 16 + 1024;  // + slack to align the base
+    // no alignment slack: the kernel requires (and checks) a 1024-byte-aligned
+    // dynamic base, which is what leaves room for P
+    static constexpr uint32_t kBytes = kMisc + 16;
 };
 
 // Reference point of the exponentials.  The online softmax of §3.2 subtracts
@@ -103,19 +103,22 @@ __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const AttnArgs args) {
     using L = AttnSmem<D>;
-    constexpr int NS = L::kStages;
+    constexpr int NSL = L::kSlots;
     constexpr int HALVES = D / 64;
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const uint32_t s_base = smem_u32(smem);
+    if ((s_base & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicOr(args.status, RA_DEV_SMEM_ALIGN_BIT);
+        return;
+    }
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-    const int B_QFULL = 0, B_KFULL = 1, B_VFULL = 1 + NS, B_KEMPTY = 1 + 2 * NS,
-              B_VEMPTY = 1 + 3 * NS, B_SFULL = 1 + 4 * NS, B_PFULL = B_SFULL + 2,
-              B_PVDONE = B_PFULL + 2, B_FINAL = B_PVDONE + 2;
+    const int B_QFULL = 0, B_SLOTF = 1, B_SLOTE = 1 + NSL, B_SFULL = 1 + 2 * NSL, B_SFREE = B_SFULL + 2,
+              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_FINAL = B_PVDONE + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
 
@@ -165,14 +168,13 @@ __global__ void __launch_bounds__(384, 1)
     // ---- setup
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QFULL), 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(BAR(B_KFULL + s), 1);
-            mbar_init(BAR(B_VFULL + s), 1);
-            mbar_init(BAR(B_KEMPTY + s), 1);
-            mbar_init(BAR(B_VEMPTY + s), 1);
+        for (int s = 0; s < NSL; ++s) {
+            mbar_init(BAR(B_SLOTF + s), 1);
+            mbar_init(BAR(B_SLOTE + s), 1);
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(BAR(B_SFULL + g), 1);
+            mbar_init(BAR(B_SFREE + g), 128);
             mbar_init(BAR(B_PFULL + g), 128);
             mbar_init(BAR(B_PVDONE + g), 1);
         }
@@ -210,65 +212,78 @@ __global__ void __launch_bounds__(384, 1)
                                 xh + 64 * c, row0 + 128 * g, zq);
         }
         __syncwarp();
-        TileWalk w = walk0;
-        w.start_step();
-        int t = 0, k_issued = 0, v_issued = 0;
+        // K and V tiles share a ring of three slots.  Load order K(0), K(1),
+        // V(0), K(2), V(1), ...: K runs a tile ahead, because S(t+1) is issued
+        // while P(t) is still being built.  Load i goes to slot i % 3 once the
+        // load three before it has been released (K after both S products of
+        // its tile, V after both PV products).
+        // one walk over the key tiles; V(t) reuses the coordinates K(t) had
+        TileWalk wk = walk0;
+        wk.start_step();
+        int vj = 0, vtile = 0;
+        int i = 0, withheld = -1;
         bool ok = true;
-        for (; w.valid(); w.next(), ++t) {
-            // K of a stage is free once both S MMAs of its tile are done, V
-            // once both PV MMAs are; K therefore refills about a tile earlier
-            const int st = t % NS;
-            const int zkv = (ring ? w.j * args.B : 0) + b;
-            const int y = w.tile * 128;
-            if (t >= NS && !(ok = warp_wait(BAR(B_KEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
-            const bool withhold = args.inject_stall && blockIdx.x == 0 && t == 1;
+        auto load = [&](int wj, int wtile, bool is_k) -> bool {
+            const int sl = i % NSL;
+            if (i >= NSL && !warp_wait(BAR(B_SLOTE + sl), ((i / NSL) - 1) & 1, abort_flag)) return false;
+            const bool withhold = args.inject_stall && blockIdx.x == 0 && i == 1;
             if (lane == 0 && !withhold) {
-                mbar_arrive_expect_tx(BAR(B_KFULL + st), L::kTile);
-                for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kK + st * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + st),
-                                xkv + 64 * c, y, zkv);
+                const uint32_t dst = s_base + L::kRing + sl * L::kTile;
+                const int zkv = (ring ? wj * args.B : 0) + b, y = wtile * 128;
+                mbar_arrive_expect_tx(BAR(B_SLOTF + sl), L::kTile);
+                for (int c = 0; c < HALVES; ++c) {
+                    if (is_k) tma_load_3d(dst + c * L::kBox, &tmk, BAR(B_SLOTF + sl), xkv + 64 * c, y, zkv);
+                    else tma_load_3d(dst + c * L::kBox, &tmv, BAR(B_SLOTF + sl), xkv + 64 * c, y, zkv);
+                }
             }
             __syncwarp();
-            if (!withhold) k_issued = t + 1;
-            if (t >= NS && !(ok = warp_wait(BAR(B_VEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(B_VFULL + st), L::kTile);
-                for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kV + st * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + st),
-                                xkv + 64 * c, y, zkv);
+            if (withhold) withheld = i;
+            ++i;
+            return true;
+        };
+        if (wk.valid()) {
+            ok = load(wk.j, wk.tile, true);
+            vj = wk.j;
+            vtile = wk.tile;
+            wk.next();
+            while (ok) {
+                const bool more = wk.valid();
+                if (more && !(ok = load(wk.j, wk.tile, true))) break;
+                if (!(ok = load(vj, vtile, false)) || !more) break;
+                vj = wk.j;
+                vtile = wk.tile;
+                wk.next();
             }
-            __syncwarp();
-            v_issued = t + 1;
         }
         if (!ok) {
             if (lane == 0) record_timeout(args.status, abort_flag);
             // let the copies already issued land before the CTA exits
             volatile int never = 0;
             mbar_wait(BAR(B_QFULL), 0, &never);
-            for (int u = (k_issued > NS ? k_issued - NS : 0); u < k_issued; ++u)
-                mbar_wait(BAR(B_KFULL + u % NS), (u / NS) & 1, &never);
-            for (int u = (v_issued > NS ? v_issued - NS : 0); u < v_issued; ++u)
-                mbar_wait(BAR(B_VFULL + u % NS), (u / NS) & 1, &never);
+            for (int u = (i > NSL ? i - NSL : 0); u < i; ++u)
+                if (u != withheld) mbar_wait(BAR(B_SLOTF + u % NSL), (u / NSL) & 1, &never);
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer
         regs_shrink<64>();
         // Issue order per key tile t (pipe order):
-        //   PV_0(t), S_0(t+1), PV_1(t), S_1(t+1)
-        // so the softmax of tile g for t+1 overlaps PV_{1-g}(t) and
-        // S_{1-g}(t+1).  S_g(t+1) overwrites the columns PV_g(t) reads P_g
-        // from, so it waits for PV_g(t) to finish.
-        // Descriptors are built once; each k-step adds a compile-time offset
-        // (16-byte units) to the start-address field: 32 B per 16-element step
-        // inside a 64-column box, one box (16 KB) for columns 64-127 of Q and
-        // K, and 16 rows (2 KB) per step of V.  The whole warp runs the issue
-        // code and elect.sync picks the issuing lane.
+        //   S_0(t+1), PV_0(t), S_1(t+1), PV_1(t)
+        // P_g goes to shared memory, so S_g(t+1) may overwrite S_g(t) in
+        // tensor memory as soon as the softmax warps of tile g are done with it
+        // (S free); nothing here waits for a PV product.  Descriptors are built
+        // once; each k-step adds a compile-time offset (16-byte units) to the
+        // start-address field: 32 B per 16-element step inside a 64-column box
+        // and one box (16 KB) for columns 64-127 of Q, K and P, and 16 rows
+        // (2 KB) per step of V.  The whole warp runs the issue code and
+        // elect.sync picks the issuing lane.
         const uint64_t dq[2] = {sdesc_sw128(s_base + L::kQ, 16, 1024),
                                 sdesc_sw128(s_base + L::kQ + L::kTile, 16, 1024)};
-        const uint64_t dk0 = sdesc_sw128(s_base + L::kK, 16, 1024);
-        const uint64_t dv0 = sdesc_sw128(s_base + L::kV, L::kBox, 1024);
-        auto issue_s = [&](int g, int stage) {
-            const uint64_t a0 = dq[g], b0 = dk0 + (uint64_t)(stage * (L::kTile >> 4));
+        const uint64_t dp[2] = {sdesc_sw128(s_base + L::kP, 16, 1024),
+                                sdesc_sw128(s_base + L::kP + 2 * L::kBox, 16, 1024)};
+        const uint64_t dk0 = sdesc_sw128(s_base + L::kRing, 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(s_base + L::kRing, L::kBox, 1024);
+        auto issue_s = [&](int g, int slot) {
+            const uint64_t a0 = dq[g], b0 = dk0 + (uint64_t)(slot * (L::kTile >> 4));
             const uint32_t d = tmem + g * 128;
             mma_ss_elect<0, 0>(d, a0, b0, IDESC_S, 0u);
             mma_ss_elect<2, 2>(d, a0, b0, IDESC_S, 1u);
@@ -283,17 +298,18 @@ __global__ void __launch_bounds__(384, 1)
             }
             tc_commit_elect(BAR(B_SFULL + g));
         };
-        auto issue_pv = [&](int g, int stage, bool first) {
-            const uint64_t b0 = dv0 + (uint64_t)(stage * (L::kTile >> 4));
-            const uint32_t d = tmem + 256 + g * D, a = tmem + g * 128;
-            mma_ts_elect<0, 0>(d, a, b0, IDESC_O, first ? 0u : 1u);
-            mma_ts_elect<8, 128>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<16, 256>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<24, 384>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<32, 512>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<40, 640>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<48, 768>(d, a, b0, IDESC_O, 1u);
-            mma_ts_elect<56, 896>(d, a, b0, IDESC_O, 1u);
+        auto issue_pv = [&](int g, int slot, bool first) {
+            constexpr uint32_t hb = L::kBox >> 4;
+            const uint64_t a0 = dp[g], b0 = dv0 + (uint64_t)(slot * (L::kTile >> 4));
+            const uint32_t d = tmem + 256 + g * D;
+            mma_ss_elect<0, 0>(d, a0, b0, IDESC_O, first ? 0u : 1u);
+            mma_ss_elect<2, 128>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<4, 256>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<6, 384>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb, 512>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 2, 640>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 4, 768>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 6, 896>(d, a0, b0, IDESC_O, 1u);
             tc_commit_elect(BAR(B_PVDONE + g));
         };
         bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
@@ -301,46 +317,44 @@ __global__ void __launch_bounds__(384, 1)
         w.start_step();
         int t = 0;
         if (ok && w.valid()) {
-            ok = warp_wait(BAR(B_KFULL + 0), 0, abort_flag);
+            ok = warp_wait(BAR(B_SLOTF + 0), 0, abort_flag);   // K(0) is load 0
             tc_fence_after();
             if (ok) {
                 issue_s(0, 0);
                 issue_s(1, 0);
-                tc_commit_elect(BAR(B_KEMPTY + 0));
+                tc_commit_elect(BAR(B_SLOTE + 0));
             }
             __syncwarp();
         }
         while (ok && w.valid()) {
-            const int st = t % NS;
-            const uint32_t ph = (t / NS) & 1;
-            const int st1 = (t + 1) % NS;
-            const uint32_t ph1 = ((t + 1) / NS) & 1;
             w.next();
             const bool has_next = w.valid();
-            if (!(ok = warp_wait(BAR(B_VFULL + st), ph, abort_flag))) break;
+            const int ki = 2 * t + 1;                        // load index of K(t+1)
+            const int vi = has_next ? 2 * t + 2 : 2 * t + 1; // load index of V(t)
+            if (has_next && !(ok = warp_wait(BAR(B_SLOTF + ki % NSL), (ki / NSL) & 1, abort_flag))) break;
+            if (has_next) {
+                if (!(ok = warp_wait(BAR(B_SFREE + 0), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_s(0, ki % NSL);
+                __syncwarp();
+            }
+            if (!(ok = warp_wait(BAR(B_SLOTF + vi % NSL), (vi / NSL) & 1, abort_flag))) break;
             if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_pv(0, st, t == 0);
+            issue_pv(0, vi % NSL, t == 0);
             __syncwarp();
             if (has_next) {
-                if (!(ok = warp_wait(BAR(B_KFULL + st1), ph1, abort_flag))) break;
-                if (!(ok = warp_wait(BAR(B_PVDONE + 0), t & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_SFREE + 1), t & 1, abort_flag))) break;
                 tc_fence_after();
-                issue_s(0, st1);
+                issue_s(1, ki % NSL);
+                tc_commit_elect(BAR(B_SLOTE + ki % NSL));
                 __syncwarp();
             }
             if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
             tc_fence_after();
-            issue_pv(1, st, t == 0);
-            tc_commit_elect(BAR(B_VEMPTY + st));
+            issue_pv(1, vi % NSL, t == 0);
+            tc_commit_elect(BAR(B_SLOTE + vi % NSL));
             __syncwarp();
-            if (has_next) {
-                if (!(ok = warp_wait(BAR(B_PVDONE + 1), t & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_s(1, st1);
-                tc_commit_elect(BAR(B_KEMPTY + st1));
-                __syncwarp();
-            }
             ++t;
         }
         if (!ok && lane == 0) record_timeout(args.status, abort_flag);
@@ -459,9 +473,11 @@ __global__ void __launch_bounds__(384, 1)
                     l *= alpha;
                     lr *= alpha;
                     m_ref = m_new;
-                    // O holds PV of every earlier tile (S_g of this tile was
-                    // computed after it); the whole warp takes part in the reload
+                    // O holds PV of every earlier tile once PV_g(t-1) is done;
+                    // the whole warp takes part in the reload
                     if (t > 0) {
+                        if (!(ok = warp_wait(BAR(B_PVDONE + g), (t - 1) & 1, abort_flag))) break;
+                        tc_fence_after();
 #pragma unroll 1
                         for (int q = 0; q < D / 16; ++q) {
                             uint32_t o[16];
@@ -471,17 +487,42 @@ __global__ void __launch_bounds__(384, 1)
                             for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                             tmem_st16(tO + q * 16, o);
                         }
+                        // PV_g(t) accumulates into O only after P full, which
+                        // follows the fence below
+                        tmem_wait_st();
                     }
                     p_pass();
                 }
             }
-            // P goes to tensor memory as 64 packed columns over S's first half
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_st16(tS + 16 * q, pr[q]);
             l += lt;
             lr += lrt;
-            tmem_wait_st();
+            // S_g(t) is no longer needed: the next S_g may overwrite it
             tc_fence_before();
+            mbar_arrive(BAR(B_SFREE + g));
+            // P_g(t) goes to shared memory -- the K-major A operand of PV in the
+            // 128-byte-swizzled layout a TMA box load would give (16-byte chunk
+            // j of row r at chunk j ^ (r mod 8); keys 0-63 in the first box) --
+            // once PV_g(t-1) has read P_g(t-1) there
+            if (t > 0 && !(ok = warp_wait(BAR(B_PVDONE + g), (t - 1) & 1, abort_flag))) break;
+            {
+                // row base (1024-byte aligned group + 128 bytes per row) and the
+                // row's chunk swizzle; both are recomputed every tile rather than
+                // kept live across the loop
+                uint32_t xr = (uint32_t)(r & 7) << 4;
+                asm volatile("" : "+r"(xr));
+                const uint32_t prow = s_base + L::kP + g * 2 * L::kBox + (r >> 3) * 1024 + xr * 8;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t off = (q >> 1) * L::kBox + ((((q & 1) * 4 + m) << 4) ^ xr);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off),
+                                     "r"(pr[q][4 * m]), "r"(pr[q][4 * m + 1]), "r"(pr[q][4 * m + 2]),
+                                     "r"(pr[q][4 * m + 3])
+                                     : "memory");
+                    }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(BAR(B_PFULL + g));
         }
         if (!ok) {
