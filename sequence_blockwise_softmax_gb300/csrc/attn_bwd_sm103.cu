@@ -36,6 +36,7 @@
 // threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
 // a tile and warps 8-11 the last 64 (no product here reduces along a row, so
 // the halves never exchange data).  Every wait is bounded.
+#include <algorithm>
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -55,7 +56,23 @@ struct BwdArgs {
     int B, S, H, Hkv, N, layout, causal;
     float scale, scale_log2;
     int n_tiles_seq;        // ceil(S / 128)
+    int bh_chunk_q;         // (batch, head) pairs interleaved heavy-first in the dQ pass
+    int bh_chunk_kv;        // (batch, key/value head) pairs, the same in the dK/dV pass
 };
+
+// Tile decode shared by both passes: (batch, head) pairs are taken in chunks
+// of `chunk` whose streamed operands fit in L2 together, and inside a chunk
+// the tiles of all its pairs are interleaved, so that the heaviest tiles of
+// every pair come first.  Returns the pair and the tile's rank within it.
+__device__ __forceinline__ void bwd_decode(int block, int per_bh, int BH, int chunk, int &bh, int &rem) {
+    const int per_chunk = chunk * per_bh;
+    const int c = block / per_chunk;
+    const int c_first = c * chunk;
+    const int c_size = min(chunk, BH - c_first);
+    const int idx = block - c * per_chunk;
+    bh = c_first + idx % c_size;
+    rem = idx / c_size;
+}
 
 __device__ __forceinline__ uint8_t *bwd_align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -215,9 +232,18 @@ __global__ void __launch_bounds__(384, 1)
 
     const int S = args.S, H = args.H, N = args.N;
     const int per_bh = N * args.n_tiles_seq;
-    const int bh = blockIdx.x / per_bh, rem = blockIdx.x % per_bh;
+    int bh, rem;
+    bwd_decode(blockIdx.x, per_bh, args.B * H, args.bh_chunk_q, bh, rem);
     const int b = bh / H, h = bh % H;
-    const int qi = rem / args.n_tiles_seq, qt = rem % args.n_tiles_seq;
+    // causal work grows with the query position: heaviest tiles first
+    int qi, qt;
+    if (args.layout == RA_CONTIGUOUS) {
+        qi = N - 1 - rem / args.n_tiles_seq;
+        qt = args.n_tiles_seq - 1 - rem % args.n_tiles_seq;
+    } else {
+        qt = args.n_tiles_seq - 1 - rem / N;
+        qi = N - 1 - rem % N;
+    }
     const int zq = qi * args.B + b;
     const int row0 = qt * 128;
     const int row_end = min(S, row0 + 128);
@@ -589,9 +615,18 @@ __global__ void __launch_bounds__(384, 1)
     const int S = args.S, H = args.H, N = args.N, Hkv = args.Hkv;
     const int group = H / Hkv;
     const int per_bh = N * args.n_tiles_seq;
-    const int bh = blockIdx.x / per_bh, rem = blockIdx.x % per_bh;
+    int bh, rem;
+    bwd_decode(blockIdx.x, per_bh, args.B * Hkv, args.bh_chunk_kv, bh, rem);
     const int b = bh / Hkv, hk = bh % Hkv;
-    const int kj = rem / args.n_tiles_seq, kt = rem % args.n_tiles_seq;
+    // causal work shrinks with the key position: earliest keys first
+    int kj, kt;
+    if (args.layout == RA_CONTIGUOUS) {
+        kj = rem / args.n_tiles_seq;
+        kt = rem % args.n_tiles_seq;
+    } else {
+        kt = rem / N;
+        kj = rem % N;
+    }
     const int zk = kj * args.B + b;
     const int c0 = kt * 128;
     const int c_end = min(S, c0 + 128);
@@ -1024,6 +1059,17 @@ ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const ch
     args.scale_log2 = args.scale * 1.4426950408889634f;
     args.n_tiles_seq = (int)((a.S + 127) / 128);
     if ((int64_t)a.N * a.B * a.S * a.H == 0) return RA_OK;
+    {
+        // bytes a tile's sweep streams per (batch, head) pair: keys + values
+        // per query head in the dQ pass (shared by a GQA group), queries + dO
+        // of the whole group per key/value head in the dK/dV pass; chunks
+        // hold about 48 MB of them (L2 holds 129 MB)
+        const int64_t group = a.H / a.H_kv;
+        const int64_t per_head = 2 * (int64_t)a.N * a.S * a.d * 2;
+        const int64_t budget = (int64_t)48 << 20;
+        args.bh_chunk_q = (int)std::max<int64_t>(1, std::min<int64_t>(budget * group / per_head, a.B * a.H));
+        args.bh_chunk_kv = (int)std::max<int64_t>(1, std::min<int64_t>(budget / (per_head * group), a.B * a.H_kv));
+    }
     return a.d == 128 ? bwd_launch_t<128>(a, args, stream, err) : bwd_launch_t<64>(a, args, stream, err);
 }
 

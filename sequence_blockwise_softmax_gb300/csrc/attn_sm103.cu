@@ -34,6 +34,7 @@
 // columns, S_g(t+1) may be computed while PV_g(t) still runs: the softmax
 // releases S_g as soon as it has read it, and each tile's critical chain is
 // S -> softmax -> PV with no wait on the previous PV in between.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 
@@ -60,6 +61,7 @@ struct AttnArgs {
     int kv_group;       // query heads per key/value head (1 without GQA)
     const int *cu_seqlens;  // packed sequences: n_seqs + 1 boundaries, or null
     int n_seqs;
+    int bh_chunk;       // (batch, head) pairs whose units are interleaved heavy-first
 };
 
 __device__ __forceinline__ void record_timeout(unsigned *status, volatile int *abort) {
@@ -125,11 +127,21 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- unit decode: heavy units first (causal work grows with position)
+    // ---- unit decode: heavy units first (causal work grows with position).
+    // The (batch, head) pairs are taken in chunks of bh_chunk whose keys and
+    // values fit in L2 together; inside a chunk the units of all its pairs are
+    // interleaved, heaviest first, so no pair's heavy units are left for the
+    // tail of the launch.
     const int S = args.S, H = args.H, N = args.N;
     const int per_bh = args.num_q_ranks * args.n_units_seq;
-    const int bh = blockIdx.x / per_bh;
-    const int rem = blockIdx.x % per_bh;
+    const int BH = args.B * H;
+    const int per_chunk = args.bh_chunk * per_bh;
+    const int chunk = blockIdx.x / per_chunk;
+    const int c_first = chunk * args.bh_chunk;
+    const int c_size = min(args.bh_chunk, BH - c_first);
+    const int idx = blockIdx.x - chunk * per_chunk;
+    const int bh = c_first + idx % c_size;
+    const int rem = idx / c_size;
     const int b = bh / H, h = bh % H;
     int qi, qt;
     if (args.layout == RA_CONTIGUOUS) {
@@ -667,6 +679,13 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     args.kv_group = (int)(a.H / (a.H_kv > 0 ? a.H_kv : a.H));
     args.cu_seqlens = a.cu_seqlens;
     args.n_seqs = a.n_seqs;
+    {
+        // keys + values one query head sweeps, shared by the heads of a GQA
+        // group; chunks hold about 48 MB of them (L2 holds 129 MB)
+        const int64_t kv_bytes = 2 * (a.ring ? a.N : 1) * a.S * a.d * 2 / args.kv_group;
+        const int64_t fit = kv_bytes > 0 ? ((int64_t)48 << 20) / kv_bytes : 1;
+        args.bh_chunk = (int)std::max<int64_t>(1, std::min<int64_t>(fit, a.B * a.H));
+    }
     const int64_t Zq = a.ring ? a.N * a.B : a.B;
     const int64_t Zkv = Zq;
     const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;
