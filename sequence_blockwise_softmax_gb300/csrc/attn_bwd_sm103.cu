@@ -16,23 +16,24 @@
 //                head of the group; the elementwise threads build P^T from
 //                S^T alone (bf16, into shared memory) and then dS^T once dP^T
 //                is there (bf16, back into tensor memory); dV += P^T dO and
-//                dK += dS^T Q accumulate in tensor memory.  Pipe order S^T(t+1),
-//                dV(t), dK(t), dP^T(t+1): with P^T in shared memory, S^T(t+1)
-//                only waits until S^T(t) is in registers, so P^T(t+1) can start
-//                as soon as dS^T(t) is done; dP^T(t+1) waits for dK(t), which
-//                reads the columns it overwrites.
+//                dK += dS^T Q accumulate in tensor memory.  With P^T in shared
+//                memory, S^T(t+1) only waits until S^T(t) is in registers, so
+//                P^T(t+1) can start as soon as dS^T(t) is done; dP^T(t+1)
+//                waits for dK(t), which reads the columns it overwrites.
 //   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
 //                visible key tile in ring order; one thread per query builds
 //                dS; dQ += dS K accumulates in tensor memory.  S/dS is double
 //                buffered and dP is taken into registers first, so S(t+1) and
-//                dP(t+1) run while dS(t) is built; pipe order S(t+1),
-//                dP(t+1), dQ(t).
+//                dP(t+1) run while dS(t) is built.
 // Masks (causal by position, packed sequences) are the forward's: in every
 // layout positions increase along a rank, so the visible partners of a row in
 // a shard form one interval of local indices.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer
-// (elect.sync), warp 2 tensor-memory allocator, warps 4-11 the elementwise
+// Warp roles (384 threads): warp 0 TMA producer, warps 1 and 3 MMA issuers
+// (elect.sync; warp 1 the products that recompute S and dP, warp 3 the
+// gradient products, so that a wait of one never holds back the other: the
+// tensor pipe takes only a few MMAs ahead of execution), warp 2
+// tensor-memory allocator, warps 4-11 the elementwise
 // threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
 // a tile and warps 8-11 the last 64 (no product here reduces along a row, so
 // the halves never exchange data).  Every wait is bounded.
@@ -201,8 +202,8 @@ struct BwdQSmem {
     static constexpr uint32_t kBars = kV + kVStages * kTile;
     // Q+dO full, K full[3], K empty[3], V full[2], V empty[2], S full[2] (one
     // per S buffer), dP full, dP free, dS full (keys 0-63), dS full (keys
-    // 64-127), dS seen by the MMA warp, dQ done, final
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 9;
+    // 64-127), dS seen by the dQ issuer, dQ done[2] (one per S buffer), final
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 10;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     static constexpr uint32_t kBytes = kMisc + 16 + 1024;
 };
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(384, 1)
     const int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + NK, B_VFULL = 1 + 2 * NK, B_VEMPTY = 1 + 2 * NK + NV,
               B_SFULL = 1 + 2 * NK + 2 * NV, B_DPFULL = B_SFULL + 2, B_DPFREE = B_SFULL + 3,
               B_DSFULL = B_SFULL + 4, B_DSFULL2 = B_SFULL + 5, B_DSACK = B_SFULL + 6,
-              B_DQDONE = B_SFULL + 7, B_FINAL = B_SFULL + 8;
+              B_DQDONE = B_SFULL + 7, B_FINAL = B_SFULL + 9;
     // tensor memory: S/dS double buffer at columns 0 and 384, dP at 128, dQ at 256
     auto s_col = [](int t) -> uint32_t { return (t & 1) ? 384u : 0u; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
@@ -287,7 +288,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(BAR(B_DSFULL2), 128);
         mbar_init(BAR(B_DSACK), 1);
         mbar_init(BAR(B_DQDONE), 1);
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_DQDONE + 1), 1);
+        mbar_init(BAR(B_FINAL), 2);   // both MMA issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -345,17 +347,19 @@ __global__ void __launch_bounds__(384, 1)
             for (int u = (v_issued > NV ? v_issued - NV : 0); u < v_issued; ++u)
                 mbar_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, &never);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------ MMA issuers
+        // Warp 1 issues S and dP, warp 3 issues dQ, so that a wait of one never
+        // holds back the other's products (the tensor pipe takes only a few
+        // MMAs ahead).  Per tile t, warp 1: dP(t+1) once the elementwise warps
+        // hold dP(t) in registers, then S(t+1) into the S buffer dQ(t-1) read
+        // dS from, once that dQ is done; warp 3: dQ(t) in two key halves as
+        // the halves of dS(t) arrive.  Each issuer commits its own products.
         const uint64_t dq_desc = sdesc_sw128(s_base + L::kQ, 16, 1024);
         const uint64_t ddo_desc = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);       // K as K-major operand
         const uint64_t dk_mn = sdesc_sw128(s_base + L::kK, L::kBox, 1024); // K as MN-major operand
         const uint64_t dv_k = sdesc_sw128(s_base + L::kV, 16, 1024);
-        // Pipe order: S(0), dP(0), then per tile t: S(t+1), dP(t+1), dQ(t).
-        // S(t+1) goes to the S buffer dQ(t-1) read dS from, so it waits for
-        // that commit; dP(t+1) overwrites dP(t), so it waits until the
-        // elementwise warps hold dP(t) in registers.
         auto issue_s = [&](int u) {
             issue_kmajor<D>(tmem + s_col(u), dq_desc, dk_k + (uint64_t)((u % NK) * (L::kTile >> 4)));
             tc_commit_elect(BAR(B_SFULL + (u & 1)));
@@ -369,46 +373,54 @@ __global__ void __launch_bounds__(384, 1)
         TileWalk w = walk0;
         w.start_step();
         int t = 0;
-        if (ok && w.valid()) {
-            ok = warp_wait(BAR(B_KFULL), 0, abort_flag) && warp_wait(BAR(B_VFULL), 0, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            __syncwarp();
-        }
-        while (ok && w.valid()) {
-            w.next();
-            const bool has_next = w.valid();
-            if (has_next) {
-                const int u = t + 1;
-                if (!(ok = warp_wait(BAR(B_KFULL + u % NK), (u / NK) & 1, abort_flag))) break;
-                if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE), (t - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_s(u);
+        if (warp == 1) {
+            if (ok && w.valid()) {
+                ok = warp_wait(BAR(B_KFULL), 0, abort_flag) && warp_wait(BAR(B_VFULL), 0, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                    issue_dp(0);
+                }
                 __syncwarp();
+            }
+            while (ok && w.valid()) {
+                w.next();
+                if (!w.valid()) break;
+                const int u = t + 1;
                 if (!(ok = warp_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, abort_flag))) break;
                 if (!(ok = warp_wait(BAR(B_DPFREE), t & 1, abort_flag))) break;
                 tc_fence_after();
                 issue_dp(u);
                 __syncwarp();
+                if (!(ok = warp_wait(BAR(B_KFULL + u % NK), (u / NK) & 1, abort_flag))) break;
+                // dQ(t-1) read dS(t-1) from this buffer (one dQ-done barrier per
+                // buffer, so neither can run two phases ahead of this wait)
+                if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag)))
+                    break;
+                tc_fence_after();
+                issue_s(u);
+                __syncwarp();
+                ++t;
             }
-            const uint64_t koff = (uint64_t)((t % NK) * (L::kTile >> 4));
-            if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_ts_half<D, 0>(tmem + 256, tmem + s_col(t), dk_mn + koff, t == 0);  // dQ += dS K, keys 0-63
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
-            if (lane == 0) mbar_arrive(BAR(B_DSACK));     // both halves of dS(t) seen
-            tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256, tmem + s_col(t) + 32, dk_mn + koff, false);   // keys 64-127
-            tc_commit_elect(BAR(B_DQDONE));
-            tc_commit_elect(BAR(B_KEMPTY + t % NK));
-            __syncwarp();
-            ++t;
+        } else {
+            for (; ok && w.valid(); w.next(), ++t) {
+                const uint64_t koff = (uint64_t)((t % NK) * (L::kTile >> 4));
+                if (!(ok = warp_wait(BAR(B_KFULL + t % NK), (t / NK) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_ts_half<D, 0>(tmem + 256, tmem + s_col(t), dk_mn + koff, t == 0);  // dQ += dS K, keys 0-63
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
+                if (lane == 0) mbar_arrive(BAR(B_DSACK));     // both halves of dS(t) seen
+                tc_fence_after();
+                issue_ts_half<D, 1>(tmem + 256, tmem + s_col(t) + 32, dk_mn + koff, false);   // keys 64-127
+                tc_commit_elect(BAR(B_DQDONE + (t & 1)));
+                tc_commit_elect(BAR(B_KEMPTY + t % NK));
+                __syncwarp();
+            }
         }
         if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+        // every product this warp issued has finished before tensor memory is freed
         __syncwarp();
         tc_commit_elect(BAR(B_FINAL));
         __syncwarp();
@@ -501,7 +513,7 @@ __global__ void __launch_bounds__(384, 1)
         } else {
             const int T = t;
             if (T > 0) {
-                ok = warp_wait(BAR(B_DQDONE), (T - 1) & 1, abort_flag);
+                ok = warp_wait(BAR(B_DQDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
                 if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
                 tc_fence_after();
             }
@@ -665,7 +677,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(BAR(B_DSFULL2), 128);
         mbar_init(BAR(B_DVDONE), 1);
         mbar_init(BAR(B_DKDONE), 1);
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_FINAL), 2);   // both MMA issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -731,19 +743,21 @@ __global__ void __launch_bounds__(384, 1)
             for (int u = (issued > NS ? issued - NS : 0); u < issued; ++u)
                 mbar_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, &never);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------ MMA issuers
         const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);
         const uint64_t dv_k = sdesc_sw128(s_base + L::kV, 16, 1024);
         const uint64_t dq_k = sdesc_sw128(s_base + L::kQ, 16, 1024);
         const uint64_t ddo_k = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dq_mn = sdesc_sw128(s_base + L::kQ, L::kBox, 1024);
         const uint64_t ddo_mn = sdesc_sw128(s_base + L::kDO, L::kBox, 1024);
-        // Pipe order: S^T(0), dP^T(0), then per query tile t: S^T(t+1), dV(t),
-        // dK(t), dP^T(t+1).  P^T lives in shared memory, so S^T(t+1) only waits
-        // until the elementwise threads hold S^T(t) in registers (S free); the
-        // whole of P(t) is built while S^T(t+1) runs.  dP^T(t+1) overwrites the
-        // columns dK(t) reads dS^T from, so it waits for dK(t)'s commit.
+        // Warp 1 issues S^T and dP^T, warp 3 dV and dK, so that a wait of one
+        // (for the next query stage, say) never holds back the other's
+        // products.  Per query tile t, warp 1: S^T(t+1) once the elementwise
+        // threads hold S^T(t) in registers (P^T lives in shared memory), then
+        // dP^T(t+1) once dK(t) has read dS^T from the columns it overwrites;
+        // warp 3: dV(t) and dK(t), each in two query halves as the halves of
+        // P^T(t) and dS^T(t) arrive.  Each issuer commits its own products.
         auto issue_sT = [&](int u) {
             issue_kmajor<D>(tmem, dk_k, dq_k + (uint64_t)((u % NS) * (L::kTile >> 4)));   // S^T = K Q^T
             tc_commit_elect(BAR(B_SFULL));
@@ -757,56 +771,59 @@ __global__ void __launch_bounds__(384, 1)
         QWalk w = walk0;
         w.start();
         int t = 0;
-        if (ok && w.valid()) {
-            ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_sT(0);
-                issue_dpT(0);
+        if (warp == 1) {
+            if (ok && w.valid()) {
+                ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sT(0);
+                    issue_dpT(0);
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        }
-        while (ok && w.valid()) {
-            const int st = t % NS;
-            const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
-            w.next();
-            const bool has_next = w.valid();
-            const int u = t + 1;
-            if (has_next) {
+            while (ok && w.valid()) {
+                w.next();
+                if (!w.valid()) break;
+                const int u = t + 1;
                 if (!(ok = warp_wait(BAR(B_SFREE), t & 1, abort_flag))) break;
                 if (!(ok = warp_wait(BAR(B_QFULL + u % NS), (u / NS) & 1, abort_flag))) break;
                 tc_fence_after();
                 issue_sT(u);
                 __syncwarp();
-            }
-            if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_ss_half<D, 0>(tmem + 256, dp_k, ddo_mn + soff, t == 0);          // dV += P^T dO
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_ss_half<D, 1>(tmem + 256, dp_k, ddo_mn + soff, false);
-            tc_commit_elect(BAR(B_DVDONE));
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128 + 32, dq_mn + soff, false);
-            tc_commit_elect(BAR(B_DKDONE));
-            tc_commit_elect(BAR(B_QEMPTY + st));
-            __syncwarp();
-            if (has_next) {
                 if (!(ok = warp_wait(BAR(B_DKDONE), t & 1, abort_flag))) break;
                 tc_fence_after();
                 issue_dpT(u);
                 __syncwarp();
+                ++t;
             }
-            ++t;
+        } else {
+            for (; ok && w.valid(); w.next(), ++t) {
+                const int st = t % NS;
+                const uint64_t soff = (uint64_t)(st * (L::kTile >> 4));
+                if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_ss_half<D, 0>(tmem + 256, dp_k, ddo_mn + soff, t == 0);          // dV += P^T dO
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_ss_half<D, 1>(tmem + 256, dp_k, ddo_mn + soff, false);
+                tc_commit_elect(BAR(B_DVDONE));
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_ts_half<D, 0>(tmem + 256 + D, tmem + 128, dq_mn + soff, t == 0); // dK += dS^T Q
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_DSFULL2), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_ts_half<D, 1>(tmem + 256 + D, tmem + 128 + 32, dq_mn + soff, false);
+                tc_commit_elect(BAR(B_DKDONE));
+                tc_commit_elect(BAR(B_QEMPTY + st));
+                __syncwarp();
+            }
         }
         if (!ok && lane == 0) bwd_timeout(args.status, abort_flag);
+        // every product this warp issued has finished before tensor memory is freed
         __syncwarp();
         tc_commit_elect(BAR(B_FINAL));
         __syncwarp();
