@@ -74,6 +74,15 @@ typedef enum {
     RA_ULYSSES_HEAD_TO_SEQ = 3   /* inverse of RA_ULYSSES_SEQ_TO_HEAD               */
 } ra_perm_op;
 
+/* Launch order.  Causal work grows with position, so the attention kernels
+ * (forward and both backward passes) run heavy units first.  They take
+ * (batch, head) pairs in chunks whose streamed keys and values (queries and dO
+ * in the dK/dV pass) fit in L2 together, about 48 MB per chunk, and
+ * interleave the units of a chunk's pairs heaviest first.  The environment
+ * variable RA_L2_CHUNK_KB, read at every launch, sets that budget in KiB (a
+ * positive integer; anything else keeps the default).  The order never
+ * changes a result: every unit's arithmetic is independent of when it runs. */
+
 /* ra_ring_attn_fwd flags */
 #define RA_FLAG_STEPWISE 1u  /* run the sweep as N x (block attention + LSE merge) */
 #define RA_FLAG_O_BF16 2u    /* write O as bf16 (rounded once, to nearest even)

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <string>
 
 #include "ra_internal.h"
@@ -66,6 +67,16 @@ ra_status check_attn_common(int64_t B, int64_t S, int64_t H, int d, int N, int l
 }  // namespace
 
 ra_status ra::set_error(ra_status st, const char *msg) { return fail(st, msg); }
+
+int64_t ra::l2_chunk_bytes() {
+    const char *e = std::getenv("RA_L2_CHUNK_KB");
+    if (e != nullptr) {
+        char *end = nullptr;
+        const long long kb = std::strtoll(e, &end, 10);
+        if (end != e && kb > 0) return (int64_t)kb << 10;
+    }
+    return (int64_t)48 << 20;
+}
 
 extern "C" {
 

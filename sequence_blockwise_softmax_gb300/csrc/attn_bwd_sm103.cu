@@ -37,7 +37,6 @@
 // threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
 // a tile and warps 8-11 the last 64 (no product here reduces along a row, so
 // the halves never exchange data).  Every wait is bounded.
-#include <algorithm>
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -1079,13 +1078,11 @@ ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const ch
     {
         // bytes a tile's sweep streams per (batch, head) pair: keys + values
         // per query head in the dQ pass (shared by a GQA group), queries + dO
-        // of the whole group per key/value head in the dK/dV pass; chunks
-        // hold about 48 MB of them (L2 holds 129 MB)
+        // of the whole group per key/value head in the dK/dV pass
         const int64_t group = a.H / a.H_kv;
         const int64_t per_head = 2 * (int64_t)a.N * a.S * a.d * 2;
-        const int64_t budget = (int64_t)48 << 20;
-        args.bh_chunk_q = (int)std::max<int64_t>(1, std::min<int64_t>(budget * group / per_head, a.B * a.H));
-        args.bh_chunk_kv = (int)std::max<int64_t>(1, std::min<int64_t>(budget / (per_head * group), a.B * a.H_kv));
+        args.bh_chunk_q = chunk_pairs(per_head / group, a.B * a.H);
+        args.bh_chunk_kv = chunk_pairs(per_head * group, a.B * a.H_kv);
     }
     return a.d == 128 ? bwd_launch_t<128>(a, args, stream, err) : bwd_launch_t<64>(a, args, stream, err);
 }

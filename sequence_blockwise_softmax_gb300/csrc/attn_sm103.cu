@@ -34,7 +34,6 @@
 // columns, S_g(t+1) may be computed while PV_g(t) still runs: the softmax
 // releases S_g as soon as it has read it, and each tile's critical chain is
 // S -> softmax -> PV with no wait on the previous PV in between.
-#include <algorithm>
 #include <cmath>
 #include <cstdio>
 
@@ -679,13 +678,9 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     args.kv_group = (int)(a.H / (a.H_kv > 0 ? a.H_kv : a.H));
     args.cu_seqlens = a.cu_seqlens;
     args.n_seqs = a.n_seqs;
-    {
-        // keys + values one query head sweeps, shared by the heads of a GQA
-        // group; chunks hold about 48 MB of them (L2 holds 129 MB)
-        const int64_t kv_bytes = 2 * (a.ring ? a.N : 1) * a.S * a.d * 2 / args.kv_group;
-        const int64_t fit = kv_bytes > 0 ? ((int64_t)48 << 20) / kv_bytes : 1;
-        args.bh_chunk = (int)std::max<int64_t>(1, std::min<int64_t>(fit, a.B * a.H));
-    }
+    // keys + values one query head sweeps, shared by the heads of a GQA group;
+    // a chunk holds about 48 MB of them by default (L2 holds 129 MB)
+    args.bh_chunk = chunk_pairs(2 * (a.ring ? a.N : 1) * a.S * a.d * 2 / args.kv_group, a.B * a.H);
     const int64_t Zq = a.ring ? a.N * a.B : a.B;
     const int64_t Zkv = Zq;
     const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;

@@ -38,6 +38,18 @@ struct AttnLaunch {
 
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);
 
+// Bytes of streamed operands per chunk of (batch, head) pairs whose units a
+// launch interleaves heaviest first (see the kernels' unit decode): the
+// RA_L2_CHUNK_KB environment variable if set to a positive number, read at
+// every launch, else 48 MiB.
+int64_t l2_chunk_bytes();
+
+// Pairs per chunk for `per_pair` streamed bytes each, between 1 and `pairs`.
+inline int chunk_pairs(int64_t per_pair, int64_t pairs) {
+    const int64_t fit = per_pair > 0 ? l2_chunk_bytes() / per_pair : pairs;
+    return (int)(fit < 1 ? 1 : (fit > pairs ? pairs : fit));
+}
+
 // One backward: D = rowsum(dO * O), then the dK / dV pass and the dQ pass.
 // q, dout: bf16 [N, B, S, H, d]; k, v: bf16 [N, B, S, H_kv, d]; o: fp32
 // [N, B, S, H, d]; lse, dvec: fp32 [N, B, H, S]; dq: fp32 like q; dk, dv:
