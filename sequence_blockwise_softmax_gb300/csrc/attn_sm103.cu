@@ -21,8 +21,12 @@
 //   warp 0      TMA producer: Q tiles once, then K and V tiles into one ring
 //               of three shared-memory slots, K a tile ahead of V.
 //   warp 1      MMA issuer (one elected lane): S_g = Q_g K^T into tensor
-//               memory, then O_g += P_g V with P_g read from shared memory.
+//               memory, and at d = 64 also O_g += P_g V with P_g read from
+//               shared memory.
 //   warp 2      tensor-memory allocator.
+//   warp 3      at d = 128, the PV issuer, so that a wait of either issuer
+//               never holds back the other's products (the tensor pipe takes
+//               only a few MMAs ahead of execution).
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
 //               query row (the 32x32b tensor-memory load gives a thread its
 //               whole row, so row sums need no shuffles), exp2 with the
@@ -78,8 +82,8 @@ struct AttnSmem {
     static constexpr uint32_t kP = kRing + kSlots * kTile;   // P_g: 128 rows x 128 keys bf16, two boxes each
     static constexpr uint32_t kBars = kP + 2 * 2 * kBox;
     // barriers: Q full, slot full[3], slot empty[3], S full[2], S free[2],
-    // P full[2], PV done[2], final
-    static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
+    // P full[2], PV done[2], final, tile count posted
+    static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
     // no alignment slack: the kernel requires (and checks) a 1024-byte-aligned
     // dynamic base, which is what leaves room for P
@@ -108,6 +112,12 @@ __global__ void __launch_bounds__(384, 1)
     constexpr int HALVES = D / 64;
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
+    // At d = 128 warp 1 issues the S products and warp 3 the PV products; at
+    // d = 64, where the split measured slower, warp 1 issues both.
+    constexpr bool TWO_ISSUERS = D == 128;
+    // registers per thread of warps 0-3 after setmaxnreg: the second issuer
+    // needs more than 64 to issue without spilling
+    constexpr uint32_t LOW_REGS = TWO_ISSUERS ? 72u : 64u;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
@@ -119,9 +129,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar0 = s_base + L::kBars;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     const int B_QFULL = 0, B_SLOTF = 1, B_SLOTE = 1 + NSL, B_SFULL = 1 + 2 * NSL, B_SFREE = B_SFULL + 2,
-              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_FINAL = B_PVDONE + 2;
+              B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_FINAL = B_PVDONE + 2, B_TCOUNT = B_FINAL + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+    volatile int *tile_count = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -189,7 +200,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(BAR(B_PFULL + g), 128);
             mbar_init(BAR(B_PVDONE + g), 1);
         }
-        mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_FINAL), TWO_ISSUERS ? 2 : 1);   // one arrival per MMA issuer
+        mbar_init(BAR(B_TCOUNT), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -209,10 +221,11 @@ __global__ void __launch_bounds__(384, 1)
 
     // 384 threads x 168 registers at launch: the producer / MMA / allocator
     // warpgroup (warps 0-3) gives registers to the two softmax warpgroups,
-    // 128 x 64 + 256 x 216 <= 384 x 168; each role makes the call on entry.
+    // 128 x LOW_REGS + 256 x 216 <= 384 x 168 (equal at LOW_REGS = 72); each
+    // role makes the call on entry.
     if (warp == 0) {
         // ================================================= TMA producer
-        regs_shrink<64>();
+        regs_shrink<LOW_REGS>();
         const int xh = h * D;                        // Q columns of head h
         const int xkv = (h / args.kv_group) * D;     // K/V columns of its key/value head
         if (lane == 0) {
@@ -274,9 +287,9 @@ __global__ void __launch_bounds__(384, 1)
             for (int u = (i > NSL ? i - NSL : 0); u < i; ++u)
                 if (u != withheld) mbar_wait(BAR(B_SLOTF + u % NSL), (u / NSL) & 1, &never);
         }
-    } else if (warp == 1) {
-        // ================================================= MMA issuer
-        regs_shrink<64>();
+    } else if (warp == 1 && !TWO_ISSUERS) {
+        // ================================================= MMA issuer (d = 64)
+        regs_shrink<LOW_REGS>();
         // Issue order per key tile t (pipe order):
         //   S_0(t+1), PV_0(t), S_1(t+1), PV_1(t)
         // P_g goes to shared memory, so S_g(t+1) may overwrite S_g(t) in
@@ -375,11 +388,146 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         volatile int never = 0;
         mbar_wait(BAR(B_FINAL), 0, &never);
+    } else if (warp == 1) {
+        // ================================================= MMA issuers (d = 128)
+        regs_shrink<LOW_REGS>();
+        // Warp 1 issues the S products and warp 3 the PV products, so that a
+        // wait of one never holds back the other (the tensor pipe takes only a
+        // few MMAs ahead of execution).  Each commits its own products: warp 1
+        // releases K slots, warp 3 V slots.
+        // Per key tile t, warp 1: S_0(t+1), S_1(t+1); warp 3: PV_0(t), PV_1(t).
+        // P_g goes to shared memory, so S_g(t+1) may overwrite S_g(t) in
+        // tensor memory as soon as the softmax warps of tile g are done with it
+        // (S free); no S product waits for a PV product.  Descriptors are built
+        // once; each k-step adds a compile-time offset (16-byte units) to the
+        // start-address field: 32 B per 16-element step inside a 64-column box
+        // and one box (16 KB) for columns 64-127 of Q, K and P, and 16 rows
+        // (2 KB) per step of V.  The whole warp runs the issue code and
+        // elect.sync picks the issuing lane.
+        const uint64_t dq[2] = {sdesc_sw128(s_base + L::kQ, 16, 1024),
+                                sdesc_sw128(s_base + L::kQ + L::kTile, 16, 1024)};
+        const uint64_t dk0 = sdesc_sw128(s_base + L::kRing, 16, 1024);
+        auto issue_s = [&](int g, int slot) {
+            const uint64_t a0 = dq[g], b0 = dk0 + (uint64_t)(slot * (L::kTile >> 4));
+            const uint32_t d = tmem + g * 128;
+            mma_ss_elect<0, 0>(d, a0, b0, IDESC_S, 0u);
+            mma_ss_elect<2, 2>(d, a0, b0, IDESC_S, 1u);
+            mma_ss_elect<4, 4>(d, a0, b0, IDESC_S, 1u);
+            mma_ss_elect<6, 6>(d, a0, b0, IDESC_S, 1u);
+            if (D == 128) {
+                constexpr uint32_t h = L::kBox >> 4;
+                mma_ss_elect<h, h>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 2, h + 2>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 4, h + 4>(d, a0, b0, IDESC_S, 1u);
+                mma_ss_elect<h + 6, h + 6>(d, a0, b0, IDESC_S, 1u);
+            }
+            tc_commit_elect(BAR(B_SFULL + g));
+        };
+        // the issuers need only the number of key tiles the walk visits,
+        // which warp 4 counts
+        bool ok = warp_wait(BAR(B_TCOUNT), 0, abort_flag);
+        const int T = ok ? *tile_count : 0;
+        ok = ok && warp_wait(BAR(B_QFULL), 0, abort_flag);
+        int t = 0;
+        if (ok && T > 0) {
+            ok = warp_wait(BAR(B_SLOTF + 0), 0, abort_flag);   // K(0) is load 0
+            tc_fence_after();
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc_commit_elect(BAR(B_SLOTE + 0));
+            }
+            __syncwarp();
+        }
+#pragma unroll 1
+        for (; ok && t + 1 < T; ++t) {
+            const int ki = 2 * t + 1;                    // load index of K(t+1)
+            if (!(ok = warp_wait(BAR(B_SLOTF + ki % NSL), (ki / NSL) & 1, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(B_SFREE + 0), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_s(0, ki % NSL);
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_SFREE + 1), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_s(1, ki % NSL);
+            tc_commit_elect(BAR(B_SLOTE + ki % NSL));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) record_timeout(args.status, abort_flag);
+        // every MMA this warp issued has finished before tensor memory is freed
+        __syncwarp();
+        tc_commit_elect(BAR(B_FINAL));
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(BAR(B_FINAL), 0, &never);
+    } else if (warp == 3 && TWO_ISSUERS) {
+        // ================================================= MMA issuer for PV (see warp 1)
+        regs_shrink<LOW_REGS>();
+        const uint64_t dp[2] = {sdesc_sw128(s_base + L::kP, 16, 1024),
+                                sdesc_sw128(s_base + L::kP + 2 * L::kBox, 16, 1024)};
+        const uint64_t dv0 = sdesc_sw128(s_base + L::kRing, L::kBox, 1024);
+        auto issue_pv = [&](int g, int slot, bool first) {
+            constexpr uint32_t hb = L::kBox >> 4;
+            const uint64_t a0 = dp[g], b0 = dv0 + (uint64_t)(slot * (L::kTile >> 4));
+            const uint32_t d = tmem + 256 + g * D;
+            mma_ss_elect<0, 0>(d, a0, b0, IDESC_O, first ? 0u : 1u);
+            mma_ss_elect<2, 128>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<4, 256>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<6, 384>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb, 512>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 2, 640>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 4, 768>(d, a0, b0, IDESC_O, 1u);
+            mma_ss_elect<hb + 6, 896>(d, a0, b0, IDESC_O, 1u);
+            tc_commit_elect(BAR(B_PVDONE + g));
+        };
+        // the issuers need only the number of key tiles the walk visits,
+        // which warp 4 counts
+        bool ok = warp_wait(BAR(B_TCOUNT), 0, abort_flag);
+        const int T = ok ? *tile_count : 0;
+        ok = ok && warp_wait(BAR(B_QFULL), 0, abort_flag);
+        int t = 0;
+#pragma unroll 1
+        for (; ok && t < T; ++t) {
+            const bool has_next = t + 1 < T;
+            const int vi = has_next ? 2 * t + 2 : 2 * t + 1; // load index of V(t)
+            if (!(ok = warp_wait(BAR(B_SLOTF + vi % NSL), (vi / NSL) & 1, abort_flag))) break;
+            if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_pv(0, vi % NSL, t == 0);
+            __syncwarp();
+            if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_pv(1, vi % NSL, t == 0);
+            tc_commit_elect(BAR(B_SLOTE + vi % NSL));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) record_timeout(args.status, abort_flag);
+        // every MMA this warp issued has finished before tensor memory is freed
+        __syncwarp();
+        tc_commit_elect(BAR(B_FINAL));
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(BAR(B_FINAL), 0, &never);
     } else if (warp < 4) {
-        regs_shrink<64>();
+        regs_shrink<LOW_REGS>();
     } else {
         // ================================================= softmax
         regs_grow<216>();
+        if (TWO_ISSUERS && warp == 4) {
+            // the number of key tiles of the walk (one step at a time), for the
+            // two MMA issuers, counted while S(0) is being computed
+            int T = 0;
+            TileWalk w = walk0;
+            for (w.start_step(); w.valid(); w.start_step()) {
+                T += w.tile_end - w.tile;
+                ++w.step;
+            }
+            if (lane == 0) {
+                *tile_count = T;
+                mbar_arrive(BAR(B_TCOUNT));
+            }
+            __syncwarp();
+        }
         const int g = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;                 // row inside Q tile g (= TMEM lane)
