@@ -29,11 +29,12 @@
 // layout positions increase along a rank, so the visible partners of a row in
 // a shard form one interval of local indices.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warps 1 and 3 MMA issuers
-// (elect.sync; warp 1 the products that recompute S and dP, warp 3 the
-// gradient products, so that a wait of one never holds back the other: the
-// tensor pipe takes only a few MMAs ahead of execution), warp 2
-// tensor-memory allocator, warps 4-11 the elementwise
+// Warp roles (384 threads): warp 0 TMA producer, warps 1-3 MMA issuers
+// (elect.sync; so that a wait of one never holds back another's products: the
+// tensor pipe takes only a few MMAs ahead of execution) -- in pass A warp 1
+// issues S^T and dP^T and warp 3 the gradient products, in pass B warp 1 dP,
+// warp 2 S and warp 3 dQ -- warp 2 also allocates tensor memory, warps 4-11
+// the elementwise
 // threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
 // a tile and warps 8-11 the last 64 (no product here reduces along a row, so
 // the halves never exchange data).  Every wait is bounded.
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(BAR(B_DSACK), 1);
         mbar_init(BAR(B_DQDONE), 1);
         mbar_init(BAR(B_DQDONE + 1), 1);
-        mbar_init(BAR(B_FINAL), 2);   // both MMA issuers
+        mbar_init(BAR(B_FINAL), 3);   // the three MMA issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -346,14 +347,14 @@ __global__ void __launch_bounds__(384, 1)
             for (int u = (v_issued > NV ? v_issued - NV : 0); u < v_issued; ++u)
                 mbar_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, &never);
         }
-    } else if (warp == 1 || warp == 3) {
+    } else if (warp >= 1 && warp <= 3) {
         // ------------------------------------------------ MMA issuers
-        // Warp 1 issues S and dP, warp 3 issues dQ, so that a wait of one never
-        // holds back the other's products (the tensor pipe takes only a few
-        // MMAs ahead).  Per tile t, warp 1: dP(t+1) once the elementwise warps
-        // hold dP(t) in registers, then S(t+1) into the S buffer dQ(t-1) read
-        // dS from, once that dQ is done; warp 3: dQ(t) in two key halves as
-        // the halves of dS(t) arrive.  Each issuer commits its own products.
+        // Warp 1 issues dP, warp 2 S and warp 3 dQ, so that a wait of one never
+        // holds back another's products (the tensor pipe takes only a few
+        // MMAs ahead).  Per tile u, warp 1: dP(u) once the elementwise warps
+        // hold dP(u-1) in registers; warp 2: S(u) into the S buffer dQ(u-2)
+        // read dS from, once that dQ is done; warp 3: dQ(u) in two key halves
+        // as the halves of dS(u) arrive.  Each issuer commits its own products.
         const uint64_t dq_desc = sdesc_sw128(s_base + L::kQ, 16, 1024);
         const uint64_t ddo_desc = sdesc_sw128(s_base + L::kDO, 16, 1024);
         const uint64_t dk_k = sdesc_sw128(s_base + L::kK, 16, 1024);       // K as K-major operand
@@ -373,33 +374,25 @@ __global__ void __launch_bounds__(384, 1)
         w.start_step();
         int t = 0;
         if (warp == 1) {
-            if (ok && w.valid()) {
-                ok = warp_wait(BAR(B_KFULL), 0, abort_flag) && warp_wait(BAR(B_VFULL), 0, abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                    issue_dp(0);
-                }
+            // dP(u) once the elementwise warps hold dP(u-1) in registers
+            for (; ok && w.valid(); w.next(), ++t) {
+                if (!(ok = warp_wait(BAR(B_VFULL + t % NV), (t / NV) & 1, abort_flag))) break;
+                if (t > 0 && !(ok = warp_wait(BAR(B_DPFREE), (t - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_dp(t);
                 __syncwarp();
             }
-            while (ok && w.valid()) {
-                w.next();
-                if (!w.valid()) break;
-                const int u = t + 1;
-                if (!(ok = warp_wait(BAR(B_VFULL + u % NV), (u / NV) & 1, abort_flag))) break;
-                if (!(ok = warp_wait(BAR(B_DPFREE), t & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_dp(u);
-                __syncwarp();
-                if (!(ok = warp_wait(BAR(B_KFULL + u % NK), (u / NK) & 1, abort_flag))) break;
-                // dQ(t-1) read dS(t-1) from this buffer (one dQ-done barrier per
-                // buffer, so neither can run two phases ahead of this wait)
-                if (t > 0 && !(ok = warp_wait(BAR(B_DQDONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag)))
+        } else if (warp == 2) {
+            // S(u) into the S buffer dQ(u-2) read dS from, once that dQ is done
+            // (one dQ-done barrier per buffer, so neither can run two phases
+            // ahead of this wait)
+            for (; ok && w.valid(); w.next(), ++t) {
+                if (!(ok = warp_wait(BAR(B_KFULL + t % NK), (t / NK) & 1, abort_flag))) break;
+                if (t > 1 && !(ok = warp_wait(BAR(B_DQDONE + ((t - 2) & 1)), ((t - 2) >> 1) & 1, abort_flag)))
                     break;
                 tc_fence_after();
-                issue_s(u);
+                issue_s(t);
                 __syncwarp();
-                ++t;
             }
         } else {
             for (; ok && w.valid(); w.next(), ++t) {
