@@ -285,6 +285,13 @@ RA_API const char *ra_last_error(void);
 /* Library version string. */
 RA_API const char *ra_version(void);
 
+/* ra_launch_chunk_pairs -- how many (batch, head) pairs the attention kernels
+ * interleave per chunk of their launch order (see "Launch order" above) when a
+ * pair streams per_pair_bytes: the budget (RA_L2_CHUNK_KB, else 48 MiB)
+ * divided by per_pair_bytes, clamped to [1, pairs].  Host only; launches
+ * nothing.  Returns 1 for per_pair_bytes <= 0 and pairs for pairs < 1. */
+RA_API int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,6 +52,7 @@ SIGNATURES = {
     "ra_check_status": (_I, [_P, _P]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),
+    "ra_launch_chunk_pairs": (_I64, [_I64, _I64]),
 }
 
 _lib = None
@@ -245,6 +246,10 @@ def ra_check_status(workspace, stream=None):
 
 def ra_version():
     return lib().ra_version().decode()
+
+
+def ra_launch_chunk_pairs(per_pair_bytes, pairs):
+    return int(lib().ra_launch_chunk_pairs(int(per_pair_bytes), int(pairs)))
 
 
 def new_workspace(nbytes, device="cuda"):

@@ -84,6 +84,13 @@ const char *ra_last_error(void) { return g_last_error.c_str(); }
 
 const char *ra_version(void) { return "ra_gb300 0.1 (sm_103a)"; }
 
+int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs) {
+    if (pairs < 1) return pairs;
+    if (per_pair_bytes <= 0) return 1;
+    const int64_t fit = ra::l2_chunk_bytes() / per_pair_bytes;
+    return fit < 1 ? 1 : (fit > pairs ? pairs : fit);
+}
+
 ra_status ra_shard_permute(const void *src, void *dst, int op, int layout, int64_t B, int64_t L,
                            int64_t H, int64_t d, int R, int U, int elem_bytes, void *stream) {
     if (op < RA_SEQ_TO_SHARDS || op > RA_ULYSSES_HEAD_TO_SEQ)

@@ -44,10 +44,10 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
 // every launch, else 48 MiB.
 int64_t l2_chunk_bytes();
 
-// Pairs per chunk for `per_pair` streamed bytes each, between 1 and `pairs`.
+// Pairs per chunk for `per_pair` streamed bytes each, between 1 and `pairs`
+// (ra_launch_chunk_pairs).
 inline int chunk_pairs(int64_t per_pair, int64_t pairs) {
-    const int64_t fit = per_pair > 0 ? l2_chunk_bytes() / per_pair : pairs;
-    return (int)(fit < 1 ? 1 : (fit > pairs ? pairs : fit));
+    return (int)ra_launch_chunk_pairs(per_pair, pairs);
 }
 
 // One backward: D = rowsum(dO * O), then the dK / dV pass and the dQ pass.

@@ -128,3 +128,21 @@ def test_workspace_sizes(ralib):
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 3) == 256 + 2 * n * 4 + 1024 * 2 * 4
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 4) == 0
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 96, 4, 0) == 0
+
+
+def test_launch_chunk_pairs(ralib, monkeypatch):
+    """The launch-order chunk: a 48 MiB budget (or RA_L2_CHUNK_KB) over the
+    bytes one (batch, head) pair streams, clamped to [1, pairs]."""
+    MiB = 1 << 20
+    monkeypatch.delenv("RA_L2_CHUNK_KB", raising=False)
+    assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3
+    assert ralib.ra_launch_chunk_pairs(64 * MiB, 8) == 1       # a 128K head: one pair per chunk
+    assert ralib.ra_launch_chunk_pairs(4 * MiB, 16) == 12      # an 8K head of config 2
+    assert ralib.ra_launch_chunk_pairs(1 * MiB, 8) == 8        # clamped to the pair count
+    assert ralib.ra_launch_chunk_pairs(0, 8) == 1
+    assert ralib.ra_launch_chunk_pairs(MiB, 0) == 0
+    monkeypatch.setenv("RA_L2_CHUNK_KB", "1536")
+    assert ralib.ra_launch_chunk_pairs(512 * 1024, 4) == 3
+    for bad in ("0", "-5", "abc", ""):
+        monkeypatch.setenv("RA_L2_CHUNK_KB", bad)
+        assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3, bad

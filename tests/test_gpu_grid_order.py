@@ -43,6 +43,10 @@ def test_chunked_order_bit_identical(ralib, gpu, monkeypatch, B, L, H, Hkv, d, N
     o0, lse0 = run_ring_gqa(ra, q, k, v, N, layout, True)
     g0 = run_bwd(ra, q, k, v, do, N, layout, True)
     monkeypatch.setenv("RA_L2_CHUNK_KB", str(kb))
+    # the forward's and the dQ pass's chunks split the pairs unevenly
+    group = H // Hkv
+    c = ra.ra_launch_chunk_pairs(4 * L * d // group, B * H)
+    assert 1 < c < B * H and (B * H) % c != 0, c
     o1, lse1 = run_ring_gqa(ra, q, k, v, N, layout, True)
     g1 = run_bwd(ra, q, k, v, do, N, layout, True)
     assert np.array_equal(o0, o1) and np.array_equal(lse0, lse1), "forward depends on the unit order"
