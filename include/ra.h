@@ -77,8 +77,9 @@ typedef enum {
 /* Launch order.  Causal work grows with position, so the attention kernels
  * (forward and both backward passes) run heavy units first.  They take
  * (batch, head) pairs in chunks whose streamed keys and values (queries and dO
- * in the dK/dV pass) fit in L2 together, about 48 MB per chunk, and
- * interleave the units of a chunk's pairs heaviest first.  The environment
+ * in the dK/dV pass) fit in L2 together, about 48 MB per chunk (all pairs
+ * at once when they fit in about 80 MB), and interleave the units of a
+ * chunk's pairs heaviest first.  The environment
  * variable RA_L2_CHUNK_KB, read at every launch, sets that budget in KiB (a
  * positive integer; anything else keeps the default).  The order never
  * changes a result: every unit's arithmetic is independent of when it runs. */
@@ -287,9 +288,12 @@ RA_API const char *ra_version(void);
 
 /* ra_launch_chunk_pairs -- how many (batch, head) pairs the attention kernels
  * interleave per chunk of their launch order (see "Launch order" above) when a
- * pair streams per_pair_bytes: the budget (RA_L2_CHUNK_KB, else 48 MiB)
- * divided by per_pair_bytes, clamped to [1, pairs].  Host only; launches
- * nothing.  Returns 1 for per_pair_bytes <= 0 and pairs for pairs < 1. */
+ * pair streams per_pair_bytes.  With B the budget (RA_L2_CHUNK_KB, else 48
+ * MiB): all pairs if they stream at most 5/3 B together (one chunk: the
+ * whole launch runs heaviest units first); otherwise the fewest chunks of at
+ * most B each, made near-equal (ceil(pairs / n) pairs for n = ceil(pairs /
+ * floor(B / per_pair_bytes))), at least 1.  Host only; launches nothing.
+ * Returns 1 for per_pair_bytes <= 0 and pairs for pairs < 1. */
 RA_API int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs);
 
 #ifdef __cplusplus

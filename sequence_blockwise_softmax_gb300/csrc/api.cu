@@ -87,8 +87,15 @@ const char *ra_version(void) { return "ra_gb300 0.1 (sm_103a)"; }
 int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs) {
     if (pairs < 1) return pairs;
     if (per_pair_bytes <= 0) return 1;
-    const int64_t fit = ra::l2_chunk_bytes() / per_pair_bytes;
-    return fit < 1 ? 1 : (fit > pairs ? pairs : fit);
+    const int64_t budget = ra::l2_chunk_bytes();
+    // every pair's operands fit in L2 together: one chunk, heaviest units first overall
+    if (per_pair_bytes <= (budget + budget * 2 / 3) / pairs) return pairs;
+    int64_t fit = budget / per_pair_bytes;
+    if (fit < 1) fit = 1;
+    if (fit >= pairs) return pairs;
+    // as many chunks as the budget needs, of near-equal size
+    const int64_t n = (pairs + fit - 1) / fit;
+    return (pairs + n - 1) / n;
 }
 
 ra_status ra_shard_permute(const void *src, void *dst, int op, int layout, int64_t B, int64_t L,

@@ -131,18 +131,22 @@ def test_workspace_sizes(ralib):
 
 
 def test_launch_chunk_pairs(ralib, monkeypatch):
-    """The launch-order chunk: a 48 MiB budget (or RA_L2_CHUNK_KB) over the
-    bytes one (batch, head) pair streams, clamped to [1, pairs]."""
+    """The launch-order chunk: all pairs when they stream at most 5/3 of the
+    budget together, else the fewest near-equal chunks of at most the budget
+    (48 MiB, or RA_L2_CHUNK_KB), clamped to [1, pairs]."""
     MiB = 1 << 20
     monkeypatch.delenv("RA_L2_CHUNK_KB", raising=False)
-    assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3
+    assert ralib.ra_launch_chunk_pairs(4 * MiB, 16) == 16      # config 2: 64 MiB in all, one chunk
+    assert ralib.ra_launch_chunk_pairs(6 * MiB, 16) == 8       # 96 MiB > 5/3 budget: 8 fit, so 8 + 8
+    assert ralib.ra_launch_chunk_pairs(16 * MiB, 64) == 3      # config 3: 3 per chunk
+    assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3       # 3 + 3 + 2
     assert ralib.ra_launch_chunk_pairs(64 * MiB, 8) == 1       # a 128K head: one pair per chunk
-    assert ralib.ra_launch_chunk_pairs(4 * MiB, 16) == 12      # an 8K head of config 2
-    assert ralib.ra_launch_chunk_pairs(1 * MiB, 8) == 8        # clamped to the pair count
+    assert ralib.ra_launch_chunk_pairs(1 * MiB, 8) == 8
     assert ralib.ra_launch_chunk_pairs(0, 8) == 1
     assert ralib.ra_launch_chunk_pairs(MiB, 0) == 0
-    monkeypatch.setenv("RA_L2_CHUNK_KB", "1536")
-    assert ralib.ra_launch_chunk_pairs(512 * 1024, 4) == 3
+    monkeypatch.setenv("RA_L2_CHUNK_KB", "1024")
+    assert ralib.ra_launch_chunk_pairs(512 * 1024, 5) == 2     # 2 + 2 + 1
+    assert ralib.ra_launch_chunk_pairs(512 * 1024, 3) == 3     # 1.5 MiB <= 5/3 MiB: one chunk
     for bad in ("0", "-5", "abc", ""):
         monkeypatch.setenv("RA_L2_CHUNK_KB", bad)
         assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3, bad

@@ -27,9 +27,9 @@ pytestmark = pytest.mark.gpu
 # 4 L d / group (forward and dQ pass) and 4 L d group (dK/dV pass): 512 KB per
 # head at L = 1024, d = 128.
 CASES = [
-    (1, 1024, 4, 4, 128, 4, "striped", 1536),     # chunks of 3 + 1 pairs, every pass
-    (1, 1024, 6, 2, 128, 4, "contiguous", 700),   # GQA: query chunks of 4 + 2
-    (2, 768, 3, 3, 64, 3, "zigzag", 800),         # B*H = 6 in chunks of 4 + 2 (192 KB per head)
+    (1, 1024, 5, 5, 128, 4, "striped", 1024),     # chunks of 2 + 2 + 1 pairs, every pass
+    (1, 1024, 9, 3, 128, 4, "contiguous", 900),   # GQA: query chunks of 5 + 4
+    (2, 768, 5, 5, 64, 3, "zigzag", 800),         # B*H = 10 in chunks of 4 + 4 + 2 (192 KB per head)
 ]
 
 
