@@ -106,7 +106,8 @@ constexpr float kSumLo = 0x1p-32f, kSumHi = 0x1p32f;
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const AttnArgs args) {
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                    const AttnArgs args) {
     using L = AttnSmem<D>;
     constexpr int NSL = L::kSlots;
     constexpr int HALVES = D / 64;
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmo);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -684,55 +686,77 @@ __global__ void __launch_bounds__(384, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(BAR(B_PFULL + g));
         }
+        const int T = t;
         if (!ok) {
             if (lane == 0) record_timeout(args.status, abort_flag);
-        } else {
-            const int T = t;
-            if (T > 0) {
-                ok = warp_wait(BAR(B_PVDONE + g), (T - 1) & 1, abort_flag);
-                if (!ok && lane == 0) record_timeout(args.status, abort_flag);
-                tc_fence_after();
-            }
-            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
-            const bool store = ok && a < S;
-            const size_t orow = ((size_t)zq * S + a) * H + h;
+        } else if (T > 0) {
+            ok = warp_wait(BAR(B_PVDONE + g), (T - 1) & 1, abort_flag);
+            if (!ok && lane == 0) record_timeout(args.status, abort_flag);
+            tc_fence_after();
+        }
+        // O_g / l goes out through shared memory and TMA: staged in this
+        // group's P buffer (and, for fp32 O at d = 128, its Q tile), both free
+        // once PV_g(T-1) is done, as boxes of 128 rows x 128 bytes in the
+        // 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r mod 8)).
+        // A unit that sees no key writes O = 0.  Every warp of the group
+        // reaches the barrier; after a timeout nothing is stored.
+        constexpr int CPB = OUT_F32 ? 32 : 64;       // O columns per box
+        constexpr int NBOX = D / CPB;
+        auto box_addr = [&](int bx) -> uint32_t {
+            return bx < 2 ? s_base + L::kP + g * 2 * L::kBox + bx * L::kBox
+                          : s_base + L::kQ + g * L::kTile + (bx - 2) * L::kBox;
+        };
+        const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+        if (ok) {
+            const uint32_t xr = (uint32_t)(r & 7) << 4;
+            const uint32_t row_off = (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
-                if (T > 0 && ok) {
+                if (T > 0) {
                     tmem_ld32(tO + q * 32, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) o[c] = 0u;
                 }
-                if (store) {
-                    if (OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.o) + orow * D + q * 32);
+                if (OUT_F32) {
+                    // 32 columns = one box, eight 16-byte chunks
+                    const uint32_t row = box_addr(q) + row_off;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
-                                                 __uint_as_float(o[4 * c + 1]) * inv_l,
-                                                 __uint_as_float(o[4 * c + 2]) * inv_l,
-                                                 __uint_as_float(o[4 * c + 3]) * inv_l);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(args.o) + orow * D + q * 32);
+                    for (int c = 0; c < 8; ++c)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c << 4) ^ xr)),
+                                     "f"(__uint_as_float(o[4 * c]) * inv_l), "f"(__uint_as_float(o[4 * c + 1]) * inv_l),
+                                     "f"(__uint_as_float(o[4 * c + 2]) * inv_l), "f"(__uint_as_float(o[4 * c + 3]) * inv_l)
+                                     : "memory");
+                } else {
+                    // 32 columns = half a box, four 16-byte chunks
+                    const uint32_t row = box_addr(q >> 1) + row_off;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 v4;
-                            v4.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
-                            v4.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
-                            v4.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
-                            v4.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
-                            dst[c] = v4;
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t w0 = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+                        const uint32_t w1 = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+                        const uint32_t w2 = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+                        const uint32_t w3 = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+                        const uint32_t chunk = (uint32_t)((q & 1) * 4 + c);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((chunk << 4) ^ xr)),
+                                     "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                                     : "memory");
                     }
                 }
             }
-            if (store)
-                args.lse[((size_t)zq * H + h) * S + a] =
-                    l > 0.f ? (m_ref + lg2(l)) * 0.6931471805599453f : -INFINITY;
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_barrier_sync(1 + g, 128);
+        if (wq == 0 && lane == 0 && *abort_flag == 0) {
+            // rows past the shard's end fall outside the tensor and are not written
+#pragma unroll
+            for (int bx = 0; bx < NBOX; ++bx) tma_store_3d(&tmo, box_addr(bx), h * D + bx * CPB, row0 + 128 * g, zq);
+            tma_store_commit();
+            tma_store_wait_read();
+        }
+        if (ok && a < S)
+            args.lse[((size_t)zq * H + h) * S + a] = l > 0.f ? (m_ref + lg2(l)) * 0.6931471805599453f : -INFINITY;
     }
 
     // ---- teardown: every role is here, all tensor-core work has finished
@@ -763,29 +787,33 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [Z, S, H*d] bf16 viewed as a 3-D tensor, 64-column x 128-row boxes with
-// the 128-byte swizzle the MMA descriptors expect.
-static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d) {
+// [Z, S, H*d] bf16 (or fp32) viewed as a 3-D tensor, boxes of 128 rows x
+// 128 bytes (64 bf16 or 32 fp32 columns) with the 128-byte swizzle the MMA
+// descriptors and the O staging expect.
+static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d,
+                     bool f32 = false) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)(H * d), (cuuint64_t)S, (cuuint64_t)Z};
-    cuuint64_t strides[2] = {(cuuint64_t)(H * d * 2), (cuuint64_t)(S * H * d * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)(H * d) * esz, (cuuint64_t)(S * H * d) * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 template <int D, bool F32>
 static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq, int64_t Zkv,
                           int64_t grid, cudaStream_t stream, const char **err) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const int64_t Hkv = a.H_kv > 0 ? a.H_kv : a.H;
     if (!make_map(&mq, a.q, Zq, a.S, a.H, D) || !make_map(&mk, a.k, Zkv, a.S, Hkv, D) ||
-        !make_map(&mv, a.v, Zkv, a.S, Hkv, D)) {
-        *err = "cuTensorMapEncodeTiled failed for the q/k/v tensor maps";
+        !make_map(&mv, a.v, Zkv, a.S, Hkv, D) || !make_map(&mo, a.o, Zq, a.S, a.H, D, F32)) {
+        *err = "cuTensorMapEncodeTiled failed for the q/k/v/o tensor maps";
         return RA_ERR_CUDA;
     }
     auto kern = attn_fwd_kernel<D, F32>;
@@ -794,7 +822,7 @@ static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq,
         *err = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
         return RA_ERR_CUDA;
     }
-    kern<<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, args);
+    kern<<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, mo, args);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         *err = cudaGetErrorString(e);
