@@ -32,12 +32,14 @@
 //               whole row, so row sums need no shuffles), exp2 with the
 //               scale folded into log2(e), P written to shared memory as
 //               bf16, O rescaled in place when the reference point moves,
-//               and the final normalisation and store.
+//               and the final normalisation, with O staged in shared memory
+//               for TMA stores.
 // Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d).  Because P does not live in S's
 // columns, S_g(t+1) may be computed while PV_g(t) still runs: the softmax
-// releases S_g as soon as it has read it, and each tile's critical chain is
-// S -> softmax -> PV with no wait on the previous PV in between.
+// releases S_g once P is computed and its denominator checked (the rare
+// second pass reloads S), and each tile's critical chain is S -> softmax ->
+// PV with no wait on the previous PV in between.
 #include <cmath>
 #include <cstdio>
 
