@@ -23,8 +23,10 @@ def _shards(ra, x, N):
     return y
 
 
-def test_withheld_tile_times_out_and_context_survives(ralib, gpu):
-    B, L, H, d, N = 1, 1024, 2, 128, 2
+# d = 128 runs two MMA issuers (S and PV), d = 64 one: both wind down on a timeout
+@pytest.mark.parametrize("d", [128, 64])
+def test_withheld_tile_times_out_and_context_survives(ralib, gpu, d):
+    B, L, H, N = 1, 1024, 2, 2
     q, k, v, _ = make_qkv(B, L, H, d, seed=71)
     qs, ks, vs = (_shards(ralib, x, N) for x in (q, k, v))
     S = L // N
