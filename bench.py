@@ -51,11 +51,36 @@ def algorithmic_flops(B, L, H, d, causal):
     return 4.0 * B * H * d * pairs
 
 
+def _code_only(text):
+    """C++ source with comments and whitespace removed, so that the hash moves only
+    when the code does.  String literals are kept whole."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join("".join(out).split())
+
+
 def kernel_source_hash():
+    """Hash of the attention kernel's code (comments and whitespace excluded)."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

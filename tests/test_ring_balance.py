@@ -50,3 +50,14 @@ def test_config4_critical_paths():
     assert zz["pairs_critical_path"] == S * S // 2 + S // 2 + 15 * S * S // 2
     assert 1.93 < con["pairs_ratio"] < 1.95
     assert st["pairs_ratio"] < 1.0002 and zz["pairs_ratio"] < 1.0002
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The DRAM-traffic figure is tied to the kernel's code: comments and
+    whitespace do not move the hash, code and string literals do."""
+    code = bench._code_only
+    a = "int a = 1; // one\n/* block\n comment */ const char *s = \"x // y\";\n"
+    b = "int a=1;\nconst char *s = \"x // y\"; // another comment\n"
+    assert code(a) == code(b)
+    assert code(a) != code(a.replace("a = 1", "a = 2"))
+    assert code(a) != code(a.replace("x // y", "x / y"))
