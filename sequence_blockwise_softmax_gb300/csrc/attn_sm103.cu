@@ -87,9 +87,51 @@ struct AttnSmem {
     // P full[2], PV done[2], final, tile count posted
     static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;
+    // the tile-skipping variant's step table: per ring step (at most
+    // kMaxSteps) the unit's key-tile range and each Q tile's own range inside
+    // it, six ints
+    static constexpr int kMaxSteps = 64;
+    static constexpr uint32_t kTab = kMisc + 16;
     // no alignment slack: the kernel requires (and checks) a 1024-byte-aligned
     // dynamic base, which is what leaves room for P
     static constexpr uint32_t kBytes = kMisc + 16;
+    static constexpr uint32_t kBytesSkip = kTab + kMaxSteps * 6 * 4;
+};
+
+// The key tiles of a unit's walk as the tile-skipping variant sees them: the
+// walk visits tiles [lo, hi) of each step's shard in step order, and Q tile g
+// needs only tiles [glo_g, ghi_g) of them.  With no table (more steps than it
+// holds) every tile is needed by both Q tiles.
+struct StepCursor {
+    const int *tab;   // null: no table
+    int ns, s, tile, hi, lo0, hi0, lo1, hi1;   // the current step's ranges
+    __device__ void seek() {
+        while (s < ns && tab[6 * s] >= tab[6 * s + 1]) ++s;
+        if (s < ns) {
+            tile = tab[6 * s];
+            hi = tab[6 * s + 1];
+            lo0 = tab[6 * s + 2];
+            hi0 = tab[6 * s + 3];
+            lo1 = tab[6 * s + 4];
+            hi1 = tab[6 * s + 5];
+        }
+    }
+    __device__ void start(const int *t, int n) {
+        tab = t;
+        ns = n;
+        s = 0;
+        tile = 0;
+        if (tab) seek();
+    }
+    __device__ void next() {
+        if (tab && ++tile >= hi) {
+            ++s;
+            seek();
+        }
+    }
+    __device__ bool need(int g) const {
+        return !tab || (g == 0 ? (lo0 <= tile && tile < hi0) : (lo1 <= tile && tile < hi1));
+    }
 };
 
 // Reference point of the exponentials.  The online softmax of §3.2 subtracts
@@ -105,7 +147,10 @@ struct AttnSmem {
 // reference never moves at all.
 constexpr float kSumLo = 0x1p-32f, kSumHi = 0x1p32f;
 
-template <int D, bool OUT_F32>
+// SKIP: each Q tile of a unit skips the key tiles none of its own rows sees
+// (packed sequences in the striped layout, where a unit's 256 rows span many
+// short sequences); the MMA issuers skip those tiles' S and PV.
+template <int D, bool OUT_F32, bool SKIP>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -121,6 +166,7 @@ __global__ void __launch_bounds__(384, 1)
     // registers per thread of warps 0-3 after setmaxnreg: the second issuer
     // needs more than 64 to issue without spilling
     constexpr uint32_t LOW_REGS = TWO_ISSUERS ? 72u : 64u;
+    static_assert(!SKIP || TWO_ISSUERS, "tile skipping is built on the two-issuer pipeline");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
@@ -136,6 +182,8 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
     volatile int *tile_count = reinterpret_cast<volatile int *>(smem + L::kMisc + 8);
+    volatile int *tab_ok = reinterpret_cast<volatile int *>(smem + L::kMisc + 12);
+    int *step_tab = reinterpret_cast<int *>(smem + L::kTab);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -428,34 +476,80 @@ __global__ void __launch_bounds__(384, 1)
             tc_commit_elect(BAR(B_SFULL + g));
         };
         // the issuers need only the number of key tiles the walk visits,
-        // which warp 4 counts
+        // which warp 4 counts (and, when skipping, its step table)
         bool ok = warp_wait(BAR(B_TCOUNT), 0, abort_flag);
         const int T = ok ? *tile_count : 0;
         ok = ok && warp_wait(BAR(B_QFULL), 0, abort_flag);
-        int t = 0;
-        if (ok && T > 0) {
-            ok = warp_wait(BAR(B_SLOTF + 0), 0, abort_flag);   // K(0) is load 0
-            tc_fence_after();
-            if (ok) {
-                issue_s(0, 0);
-                issue_s(1, 0);
-                tc_commit_elect(BAR(B_SLOTE + 0));
+        if constexpr (!SKIP) {
+            int t = 0;
+            if (ok && T > 0) {
+                ok = warp_wait(BAR(B_SLOTF + 0), 0, abort_flag);   // K(0) is load 0
+                tc_fence_after();
+                if (ok) {
+                    issue_s(0, 0);
+                    issue_s(1, 0);
+                    tc_commit_elect(BAR(B_SLOTE + 0));
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        }
 #pragma unroll 1
-        for (; ok && t + 1 < T; ++t) {
-            const int ki = 2 * t + 1;                    // load index of K(t+1)
-            if (!(ok = warp_wait(BAR(B_SLOTF + ki % NSL), (ki / NSL) & 1, abort_flag))) break;
-            if (!(ok = warp_wait(BAR(B_SFREE + 0), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_s(0, ki % NSL);
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_SFREE + 1), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_s(1, ki % NSL);
-            tc_commit_elect(BAR(B_SLOTE + ki % NSL));
-            __syncwarp();
+            for (; ok && t + 1 < T; ++t) {
+                const int ki = 2 * t + 1;                    // load index of K(t+1)
+                if (!(ok = warp_wait(BAR(B_SLOTF + ki % NSL), (ki / NSL) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_SFREE + 0), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_s(0, ki % NSL);
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_SFREE + 1), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_s(1, ki % NSL);
+                tc_commit_elect(BAR(B_SLOTE + ki % NSL));
+                __syncwarp();
+            }
+        } else {
+            // S_g is issued only for the tiles Q tile g needs; each group's
+            // S-free wait counts that group's own products.  A K slot is
+            // released after its tile, whether or not any S read it.
+            StepCursor cs;
+            cs.start((ok && *tab_ok) ? step_tab : nullptr, args.num_steps);
+            int ks0 = 0, ks1 = 0;         // S products issued per Q tile
+            if (ok && T > 0) {
+                ok = warp_wait(BAR(B_SLOTF + 0), 0, abort_flag);   // K(0) is load 0
+                tc_fence_after();
+                if (ok) {
+                    if (cs.need(0)) {
+                        issue_s(0, 0);
+                        ++ks0;
+                    }
+                    if (cs.need(1)) {
+                        issue_s(1, 0);
+                        ++ks1;
+                    }
+                    tc_commit_elect(BAR(B_SLOTE + 0));
+                }
+                __syncwarp();
+            }
+#pragma unroll 1
+            for (int t = 0; ok && t + 1 < T; ++t) {
+                cs.next();
+                const int ki = 2 * t + 1;                    // load index of K(t+1)
+                if (!(ok = warp_wait(BAR(B_SLOTF + ki % NSL), (ki / NSL) & 1, abort_flag))) break;
+                if (cs.need(0)) {
+                    if (ks0 > 0 && !(ok = warp_wait(BAR(B_SFREE + 0), (ks0 - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_s(0, ki % NSL);
+                    ++ks0;
+                    __syncwarp();
+                }
+                if (cs.need(1)) {
+                    if (ks1 > 0 && !(ok = warp_wait(BAR(B_SFREE + 1), (ks1 - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_s(1, ki % NSL);
+                    ++ks1;
+                }
+                tc_commit_elect(BAR(B_SLOTE + ki % NSL));
+                __syncwarp();
+            }
         }
         if (!ok && lane == 0) record_timeout(args.status, abort_flag);
         // every MMA this warp issued has finished before tensor memory is freed
@@ -485,25 +579,55 @@ __global__ void __launch_bounds__(384, 1)
             tc_commit_elect(BAR(B_PVDONE + g));
         };
         // the issuers need only the number of key tiles the walk visits,
-        // which warp 4 counts
+        // which warp 4 counts (and, when skipping, its step table)
         bool ok = warp_wait(BAR(B_TCOUNT), 0, abort_flag);
         const int T = ok ? *tile_count : 0;
         ok = ok && warp_wait(BAR(B_QFULL), 0, abort_flag);
-        int t = 0;
+        if constexpr (!SKIP) {
+            int t = 0;
 #pragma unroll 1
-        for (; ok && t < T; ++t) {
-            const bool has_next = t + 1 < T;
-            const int vi = has_next ? 2 * t + 2 : 2 * t + 1; // load index of V(t)
-            if (!(ok = warp_wait(BAR(B_SLOTF + vi % NSL), (vi / NSL) & 1, abort_flag))) break;
-            if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_pv(0, vi % NSL, t == 0);
-            __syncwarp();
-            if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_pv(1, vi % NSL, t == 0);
-            tc_commit_elect(BAR(B_SLOTE + vi % NSL));
-            __syncwarp();
+            for (; ok && t < T; ++t) {
+                const bool has_next = t + 1 < T;
+                const int vi = has_next ? 2 * t + 2 : 2 * t + 1; // load index of V(t)
+                if (!(ok = warp_wait(BAR(B_SLOTF + vi % NSL), (vi / NSL) & 1, abort_flag))) break;
+                if (!(ok = warp_wait(BAR(B_PFULL + 0), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_pv(0, vi % NSL, t == 0);
+                __syncwarp();
+                if (!(ok = warp_wait(BAR(B_PFULL + 1), t & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_pv(1, vi % NSL, t == 0);
+                tc_commit_elect(BAR(B_SLOTE + vi % NSL));
+                __syncwarp();
+            }
+        } else {
+            // PV_g only for the tiles Q tile g needs; P-full waits and the
+            // accumulate flag count that group's own products
+            StepCursor cv;
+            cv.start((ok && *tab_ok) ? step_tab : nullptr, args.num_steps);
+            int kv0 = 0, kv1 = 0;         // PV products issued per Q tile
+#pragma unroll 1
+            for (int t = 0; ok && t < T; ++t) {
+                const bool has_next = t + 1 < T;
+                const int vi = has_next ? 2 * t + 2 : 2 * t + 1; // load index of V(t)
+                if (!(ok = warp_wait(BAR(B_SLOTF + vi % NSL), (vi / NSL) & 1, abort_flag))) break;
+                if (cv.need(0)) {
+                    if (!(ok = warp_wait(BAR(B_PFULL + 0), kv0 & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(0, vi % NSL, kv0 == 0);
+                    ++kv0;
+                    __syncwarp();
+                }
+                if (cv.need(1)) {
+                    if (!(ok = warp_wait(BAR(B_PFULL + 1), kv1 & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(1, vi % NSL, kv1 == 0);
+                    ++kv1;
+                }
+                tc_commit_elect(BAR(B_SLOTE + vi % NSL));
+                __syncwarp();
+                cv.next();
+            }
         }
         if (!ok && lane == 0) record_timeout(args.status, abort_flag);
         // every MMA this warp issued has finished before tensor memory is freed
@@ -519,15 +643,68 @@ __global__ void __launch_bounds__(384, 1)
         regs_grow<216>();
         if (TWO_ISSUERS && warp == 4) {
             // the number of key tiles of the walk (one step at a time), for the
-            // two MMA issuers, counted while S(0) is being computed
+            // two MMA issuers, counted while S(0) is being computed.  The
+            // tile-skipping variant also writes the step table: for each ring
+            // step (one lane per step) the unit's key-tile range and each Q
+            // tile's own range inside it, from its first row's sequence start
+            // to its last row (or that row's sequence end without the causal
+            // mask).  Past kMaxSteps steps there is no table and every tile
+            // counts for both Q tiles.
             int T = 0;
-            TileWalk w = walk0;
-            for (w.start_step(); w.valid(); w.start_step()) {
-                T += w.tile_end - w.tile;
-                ++w.step;
+            bool have_tab = false;
+            if constexpr (SKIP) have_tab = args.num_steps <= L::kMaxSteps;
+            if (have_tab) {
+                int64_t glo_pos[2], ghi_pos[2];
+                bool gvalid[2];
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {
+                    const int fr = row0 + 128 * gg, lrow = min(S, fr + 128) - 1;
+                    gvalid[gg] = fr < S;
+                    const int64_t fp = token_pos(args.layout, q_rank, gvalid[gg] ? fr : 0, N, S);
+                    const int64_t lp = token_pos(args.layout, q_rank, gvalid[gg] ? lrow : 0, N, S);
+                    int64_t fs, fe, ls, le;
+                    seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, fp, fs, fe);
+                    seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, lp, ls, le);
+                    glo_pos[gg] = fs - 1;
+                    ghi_pos[gg] = args.causal ? lp : le - 1;
+                }
+                for (int s0 = 0; s0 < args.num_steps; s0 += 32) {
+                    const int st = s0 + lane;
+                    int cnt = 0;
+                    if (st < args.num_steps) {
+                        const int j = walk0.kv_fixed >= 0 ? walk0.kv_fixed
+                                                          : ((q_rank - st - walk0.step_base) % N + N) % N;
+                        const int ulo = (int)(keys_upto(args.layout, j, walk0.lo_pos, N, S) / 128);
+                        const int uhi =
+                            max(ulo, (int)((keys_upto(args.layout, j, walk0.hi_pos, N, S) + 127) / 128));
+                        int e[6] = {ulo, uhi, ulo, ulo, ulo, ulo};
+#pragma unroll
+                        for (int gg = 0; gg < 2; ++gg)
+                            if (gvalid[gg]) {
+                                const int lo = (int)(keys_upto(args.layout, j, glo_pos[gg], N, S) / 128);
+                                const int hi = (int)((keys_upto(args.layout, j, ghi_pos[gg], N, S) + 127) / 128);
+                                e[2 + 2 * gg] = max(lo, ulo);
+                                e[3 + 2 * gg] = max(e[2 + 2 * gg], min(hi, uhi));
+                            }
+#pragma unroll
+                        for (int c = 0; c < 6; ++c) step_tab[6 * st + c] = e[c];
+                        cnt = uhi - ulo;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+                    T += cnt;
+                }
+            } else {
+                TileWalk w = walk0;
+                for (w.start_step(); w.valid(); w.start_step()) {
+                    T += w.tile_end - w.tile;
+                    ++w.step;
+                }
             }
+            __syncwarp();
             if (lane == 0) {
                 *tile_count = T;
+                if constexpr (SKIP) *tab_ok = have_tab ? 1 : 0;
                 mbar_arrive(BAR(B_TCOUNT));
             }
             __syncwarp();
@@ -552,15 +729,27 @@ __global__ void __launch_bounds__(384, 1)
         const int64_t my_hi_pos = args.causal ? my_pos : my_end - 1;
         TileWalk w = walk0;
         w.start_step();
-        int t = 0;
+        int t = 0;              // key tiles this Q tile has processed
         bool ok = true;
+        bool have_tab = false;  // tile skipping: the step table was written
+        if constexpr (SKIP) {
+            ok = warp_wait(BAR(B_TCOUNT), 0, abort_flag);
+            have_tab = ok && *tab_ok != 0;
+        }
         int cur_step = -1;
         int klo = 0, khi = S;   // this row's visible local keys [klo, khi) of shard w.j
-        for (; w.valid(); w.next(), ++t) {
+        // (t counts the tiles processed: without skipping, every tile the walk visits)
+        for (; (!SKIP || ok) && w.valid(); w.next(), t += SKIP ? 0 : 1) {
             if (w.step != cur_step) {
                 cur_step = w.step;
                 klo = (int)keys_upto(args.layout, w.j, my_lo_pos, N, S);
                 khi = (int)keys_upto(args.layout, w.j, my_hi_pos, N, S);
+            }
+            // a tile no row of this Q tile sees (the tiles of shard w.j it
+            // sees are [e[0], e[1])): the MMA issuers skip its S and PV too
+            if (SKIP && have_tab) {
+                const int *e = step_tab + 6 * w.step + 2 + 2 * g;
+                if (w.tile < e[0] || w.tile >= e[1]) continue;
             }
             if (!(ok = warp_wait(BAR(B_SFULL + g), t & 1, abort_flag))) break;
             tc_fence_after();
@@ -687,6 +876,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(BAR(B_PFULL + g));
+            if constexpr (SKIP) ++t;
         }
         const int T = t;
         if (!ok) {
@@ -808,7 +998,7 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, i
     return r == CUDA_SUCCESS;
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool SKIP>
 static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq, int64_t Zkv,
                           int64_t grid, cudaStream_t stream, const char **err) {
     CUtensorMap mq, mk, mv, mo;
@@ -818,8 +1008,8 @@ static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq,
         *err = "cuTensorMapEncodeTiled failed for the q/k/v/o tensor maps";
         return RA_ERR_CUDA;
     }
-    auto kern = attn_fwd_kernel<D, F32>;
-    const int smem = (int)AttnSmem<D>::kBytes;
+    auto kern = attn_fwd_kernel<D, F32, SKIP>;
+    const int smem = (int)(SKIP ? AttnSmem<D>::kBytesSkip : AttnSmem<D>::kBytes);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
         *err = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
         return RA_ERR_CUDA;
@@ -867,11 +1057,20 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
         *err = "too many query tiles for one launch";
         return RA_ERR_UNSUPPORTED;
     }
+    // Packed sequences in the striped layout take the tile-skipping variant
+    // (d = 128): there a unit's 256 rows span N x 256 positions, many short
+    // sequences, and each Q tile sees few of the tiles the unit visits.
+    // Elsewhere skipping removes little work and measured slower (zigzag
+    // packed sequences too).
+    const bool skip = a.d == 128 && a.cu_seqlens != nullptr && a.layout == RA_STRIPED;
+    if (skip)
+        return a.out_f32 ? launch_t<128, true, true>(a, args, Zq, Zkv, grid, stream, err)
+                         : launch_t<128, false, true>(a, args, Zq, Zkv, grid, stream, err);
     if (a.d == 128)
-        return a.out_f32 ? launch_t<128, true>(a, args, Zq, Zkv, grid, stream, err)
-                         : launch_t<128, false>(a, args, Zq, Zkv, grid, stream, err);
-    return a.out_f32 ? launch_t<64, true>(a, args, Zq, Zkv, grid, stream, err)
-                     : launch_t<64, false>(a, args, Zq, Zkv, grid, stream, err);
+        return a.out_f32 ? launch_t<128, true, false>(a, args, Zq, Zkv, grid, stream, err)
+                         : launch_t<128, false, false>(a, args, Zq, Zkv, grid, stream, err);
+    return a.out_f32 ? launch_t<64, true, false>(a, args, Zq, Zkv, grid, stream, err)
+                     : launch_t<64, false, false>(a, args, Zq, Zkv, grid, stream, err);
 }
 
 }  // namespace ra

@@ -47,6 +47,13 @@ CASES = [
     (768, 2, 2, 128, 2, "striped", False, "random4"),
     (2048, 2, 1, 128, 4, "zigzag", True, "random33"),
     (1024, 2, 2, 128, 4, "striped", True, [0, 1024]),                          # one sequence
+    # many short sequences: each 128-row Q tile of a unit sees only some of
+    # the tiles the unit visits, so d = 128 striped / zigzag skip tiles per Q tile
+    (8192, 2, 1, 128, 4, "striped", True, "random64"),
+    (6144, 2, 2, 128, 3, "zigzag", True, "random48"),
+    (4096, 2, 2, 128, 4, "striped", False, "random20"),
+    # more ring steps than the skip table holds: every tile is visited
+    (9216, 1, 1, 128, 72, "striped", True, "random30"),
 ]
 
 
