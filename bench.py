@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from synthetic_inputs import WORKLOADS, make_cu_seqlens, make_qkv  # noqa: E402
+from synthetic_inputs import WORKLOADS, make_cu_seqlens, make_dout, make_qkv  # noqa: E402
 
 METRIC = "causal ring-attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
 METRIC_BWD = "causal ring-attention bwd TFLOP/s (bf16, 1×GB300; algorithmic 8·B·H·d·pairs)"
@@ -260,9 +260,7 @@ class Workload:
         if self.U != 1 or self.cu is not None:
             raise ValueError("the backward bench runs plain ring layouts")
         self.step()
-        g = torch.Generator().manual_seed(7)
-        do = torch.randn((B, L, H, d), generator=g).to(torch.bfloat16)
-        self.do_seq = do.to(self.dev)
+        self.do_seq = make_dout(B, L, H, d).to(self.dev)
         self.do_shard = torch.empty_like(self.shard[0])
         S = L // N
         self.dq = torch.empty((N, B, S, H, d), dtype=torch.float32, device=self.dev)

@@ -60,3 +60,55 @@ def attention_backward(q, k, v, do, causal, scale=None, cu_seqlens=None):
             dq[b, :, h] = dS @ k[b, :, kv] * scale
             dk[b, :, kv] += dS.T @ q[b, :, h] * scale
     return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, do, causal, b, h, rows, scale=None, cu_seqlens=None, chunk=64):
+    """The same derivative restricted to the query rows ``rows`` of batch b and
+    query head h, for inputs too long for the [L, L] matrices.
+
+    A query row's softmax, dP, dS and dQ depend only on that row and all keys,
+    so each row is computed whole (every visible key in one product); rows are
+    taken ``chunk`` at a time only to bound memory.  Returns
+        dq      [len(rows), d]   exact dQ of those rows,
+        dk_part [L, d]           sum over those rows of dS[row, key] * q_row * scale,
+        dv_part [L, d]           sum over those rows of P[row, key] * dO_row,
+    the rows' contributions to dK and dV of key/value head h // (H / Hkv).  A
+    key every one of whose seeing rows (over all query heads of the group) is
+    passed gets its exact dK and dV as the sum of those contributions.
+    """
+    B, L, H, d = q.shape
+    Hkv = k.shape[2]
+    kv = h // (H // Hkv)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.asarray(rows, dtype=np.int64)
+    kk = _f64(k[b, :, kv])
+    vv = _f64(v[b, :, kv])
+    seg = None
+    if cu_seqlens is not None:
+        seg = np.searchsorted(np.asarray(cu_seqlens), np.arange(L), side="right") - 1
+    keys = np.arange(L)
+    dq = np.zeros((len(rows), d))
+    dk_part = np.zeros((L, d))
+    dv_part = np.zeros((L, d))
+    for c0 in range(0, len(rows), chunk):
+        r = rows[c0:c0 + chunk]
+        qr = _f64(q[b, r, h])
+        dor = _f64(do[b, r, h])
+        allowed = np.ones((len(r), L), dtype=bool)
+        if causal:
+            allowed &= keys[None, :] <= r[:, None]
+        if seg is not None:
+            allowed &= seg[None, :] == seg[r][:, None]
+        s = np.where(allowed, (qr @ kk.T) * scale, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        m = np.where(np.isfinite(m), m, 0.0)
+        e = np.exp(s - m)
+        den = e.sum(axis=1, keepdims=True)
+        p = np.where(den > 0, e / np.where(den > 0, den, 1.0), 0.0)
+        dP = dor @ vv.T
+        dS = p * (dP - (p * dP).sum(axis=1, keepdims=True))
+        dq[c0:c0 + len(r)] = dS @ kk * scale
+        dk_part += dS.T @ qr * scale
+        dv_part += p.T @ dor
+    return dq, dk_part, dv_part

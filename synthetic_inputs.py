@@ -89,6 +89,12 @@ def make_extreme_qkv(B, L, H, d, seed, mode):
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
+def make_dout(B, L, H, d, seed=7):
+    """The output gradient dO [B, L, H, d] bf16 of the backward workloads, N(0, 1)."""
+    g = torch.Generator().manual_seed(int(seed))
+    return torch.randn((B, L, H, d), generator=g).to(torch.bfloat16)
+
+
 def randn_bf16(shape, seed):
     """One bf16 tensor from N(0, 1) with its own seeded generator."""
     g = torch.Generator().manual_seed(int(seed))

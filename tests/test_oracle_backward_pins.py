@@ -79,3 +79,34 @@ def test_backward_catches_planted_transpose():
     dS = p * (dP - (p * dP).sum(1, keepdims=True))
     wrong = dS @ q[0, :, 0] / 2.0
     assert np.abs(wrong - dk[0, :, 0]).max() > 1e-3
+
+
+@pytest.mark.parametrize("causal,Hkv,cu", [(True, 4, None), (False, 2, None), (True, 1, [0, 17, 18, 40, 70])])
+def test_backward_rows_matches_full_backward(causal, Hkv, cu):
+    """The row-restricted backward (used at sizes where [L, L] does not fit) against the
+    full one, itself pinned by finite differences above: dQ of any rows; with every row
+    of every query head of a group passed, dK and dV of the group's key/value head; and
+    with causal masking, the exact dK / dV of the last keys from the rows that see them."""
+    from oracle.backward import attention_backward_rows
+    B, L, H, d = 2, 70, 4, 8
+    q, do = (randn_bf16((B, L, H, d), s) for s in (21, 22))
+    k, v = (randn_bf16((B, L, Hkv, d), s) for s in (23, 24))
+    dq, dk, dv = attention_backward(q, k, v, do, causal, cu_seqlens=cu)
+    group = H // Hkv
+    rows = np.array([0, 1, 5, 17, 18, 39, 40, 69])
+    for b in range(B):
+        for h in range(H):
+            dq_r, _, _ = attention_backward_rows(q, k, v, do, causal, b, h, rows, cu_seqlens=cu, chunk=3)
+            np.testing.assert_allclose(dq_r, dq[b, rows, h], rtol=0, atol=1e-12)
+        for kv in range(Hkv):
+            heads = range(kv * group, (kv + 1) * group)
+            parts = [attention_backward_rows(q, k, v, do, causal, b, h, np.arange(L), cu_seqlens=cu)
+                     for h in heads]
+            np.testing.assert_allclose(sum(p[1] for p in parts), dk[b, :, kv], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(sum(p[2] for p in parts), dv[b, :, kv], rtol=0, atol=1e-12)
+            if causal:
+                k0 = L - 9
+                tail = [attention_backward_rows(q, k, v, do, causal, b, h, np.arange(k0, L), cu_seqlens=cu)
+                        for h in heads]
+                np.testing.assert_allclose(sum(p[1] for p in tail)[k0:], dk[b, k0:, kv], rtol=0, atol=1e-12)
+                np.testing.assert_allclose(sum(p[2] for p in tail)[k0:], dv[b, k0:, kv], rtol=0, atol=1e-12)
