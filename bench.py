@@ -172,7 +172,8 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- the GPU path
 class Workload:
-    def __init__(self, ra, name, layout, dev, shape=None, stepwise=False, kv_heads=None, varlen=None):
+    def __init__(self, ra, name, layout, dev, shape=None, stepwise=False, kv_heads=None, varlen=None,
+                 seq_order=True):
         w = dict(WORKLOADS[name])
         if shape is not None:
             w.update(B=shape[0], L=shape[1], H=shape[2], d=shape[3], N=shape[4])
@@ -182,6 +183,11 @@ class Workload:
         self.causal = w["causal"]
         B, L, H, d, N, U = self.B, self.L, self.H, self.d, self.N, self.U
         self.Hkv = kv_heads or H
+        # token-order sweep (RA_FLAG_SEQ_ORDER): the layout is the tiles' addresses and no
+        # permute runs; the Ulysses split, the stepwise sweep and zigzag chunks that are not
+        # a multiple of 128 rows take the explicit permutes
+        self.seq_order = (seq_order and U == 1 and not stepwise and
+                          not (layout == "zigzag" and (L // N // 2) % 128))
         q, k, v, _ = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])
         if self.Hkv != H:
             # grouped-query attention: the first H_kv heads of the drawn K and V
@@ -205,7 +211,7 @@ class Workload:
         self.lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
         self.o_host = torch.empty((B, L, H, d), dtype=torch.float32).pin_memory()
         self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
-        self.flags = ra.RA_FLAG_STEPWISE if stepwise else 0
+        self.flags = ra.RA_FLAG_STEPWISE if stepwise else (ra.RA_FLAG_SEQ_ORDER if self.seq_order else 0)
         self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N, self.flags),
                                    device=dev)
         self.flops = algorithmic_flops(B, L, H, d, self.causal)
@@ -220,11 +226,28 @@ class Workload:
             self.cu = cu.to(torch.int32).to(dev)
         attn_launches = (2 * N - 1) if stepwise else 1     # N block sweeps + N-1 merges
         self.launches = 3 * (2 if U > 1 else 1) + attn_launches + (2 if U > 1 else 1) + 1
+        if self.seq_order:
+            self.launches = 1
         self.attn_events = []
 
     def step(self, time_attention=False, slot=0):
         ra, B, L, H, d, N, U = self.ra, self.B, self.L, self.H, self.d, self.N, self.U
         seq, o_seq, lse_seq = self.slots[slot] if slot else (self.seq, self.o_seq, self.lse_seq)
+        if self.seq_order:
+            # one launch: the sweep reads q/k/v and writes O / LSE in token order
+            if time_attention:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            if self.cu is not None:
+                ra.ra_ring_attn_fwd_varlen(*seq, o_seq, lse_seq, self.cu, L, H, self.Hkv, d, N, self.layout,
+                                           self.causal, flags=self.flags, workspace=self.ws)
+            else:
+                ra.ra_ring_attn_fwd_gqa(*seq, o_seq, lse_seq, B, L, H, self.Hkv, d, N, self.layout, self.causal,
+                                        flags=self.flags, workspace=self.ws)
+            if time_attention:
+                e1.record()
+                self.attn_events.append((e0, e1))
+            return
         for i in range(3):
             hx = self.heads[i]
             ra.ra_shard_permute(seq[i], self.shard[i], ra.RA_SEQ_TO_SHARDS, self.layout, B, L, hx, d, N, U)
@@ -525,6 +548,9 @@ def main():
                     help="run the sweep as N block launches + N-1 LSE merges (the pages' per-step loop)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward (ra_ring_attn_bwd) on saved forward outputs instead")
+    ap.add_argument("--explicit-permutes", action="store_true",
+                    help="run the forward on shard stacks with the permute kernels around the sweep "
+                         "instead of the token-order sweep")
     ap.add_argument("--varlen", type=int, default=None,
                     help="pack this many variable-length sequences (seeded cut points) into the workload")
     ap.add_argument("--kv-heads", type=int, default=None,
@@ -552,7 +578,7 @@ def main():
     layout = args.layout or w["layouts"][0]
     shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
     wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise, kv_heads=args.kv_heads,
-                  varlen=args.varlen)
+                  varlen=args.varlen, seq_order=not (args.explicit_permutes or args.backward))
 
     step = wl.step
     if args.backward:
@@ -600,6 +626,8 @@ def main():
                    "packed_sequences": args.varlen,
                    "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
                    "sweep": "stepwise" if args.stepwise else "fused",
+                   "io": ("token order: the layout is the sweep's tile addressing, no permute kernels"
+                          if wl.seq_order else "shard stacks with explicit permute kernels"),
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -88,6 +88,16 @@ typedef enum {
 #define RA_FLAG_STEPWISE 1u  /* run the sweep as N x (block attention + LSE merge) */
 #define RA_FLAG_O_BF16 2u    /* write O as bf16 (rounded once, to nearest even)
                                 instead of the default fp32 accumulator         */
+/* Sequence order: q, k, v and o are the full-sequence tensors [B, L, H, d]
+ * ([B, L, H_kv, d] for k and v) in token order and lse is [B, H, L], instead
+ * of shard stacks.  The fused sweep reads each rank's shard and writes its
+ * result straight from and to token order, the layout ([USP] §4, §6.1) being
+ * the tiles' addresses, so no permute runs: the same results as
+ * ra_shard_permute(RA_SEQ_TO_SHARDS) + the sweep + RA_SHARDS_TO_SEQ and
+ * ra_lse_to_seq, bit for bit.  Fused sweep only (not with RA_FLAG_STEPWISE);
+ * zigzag needs its chunk L / 2N to be a multiple of 128 (RA_ERR_UNSUPPORTED
+ * otherwise).  There is no Ulysses split in this form (U = 1).            */
+#define RA_FLAG_SEQ_ORDER 4u
 /* Test hook for the timeout path: the first CTA of the fused sweep never
  * loads one key tile, so the waits that depend on it run out after about two
  * seconds; the kernel records RA_ERR_TIMEOUT in the status word, releases what
@@ -169,8 +179,9 @@ RA_API ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, co
  * o: [N, B, S, H, d], fp32 by default (the fp32 accumulator itself), bf16
  * with RA_FLAG_O_BF16; lse: fp32 [N, B, H, S] (natural log).
  * Requires N | L, 2N | L for zigzag, d in {64, 128}.  scale <= 0 selects
- * 1/sqrt(d).  flags: any of RA_FLAG_STEPWISE, RA_FLAG_O_BF16 (and the test
- * hook RA_FLAG_INJECT_STALL, fused sweep only).  workspace:
+ * 1/sqrt(d).  flags: any of RA_FLAG_STEPWISE, RA_FLAG_O_BF16, RA_FLAG_SEQ_ORDER
+ * (which changes the q/k/v/o/lse layouts to token order, see there; and the
+ * test hook RA_FLAG_INJECT_STALL, fused sweep only).  workspace:
  * device, ra_ring_attn_workspace_bytes() bytes, zero-filled before its first
  * use.
  */
@@ -208,7 +219,9 @@ RA_API ra_status ra_ring_attn_fwd_gqa(const void *q, const void *k, const void *
  * allowed).  The layout shards the packed stream by global position; a query
  * sees only keys of its own sequence (and, causal, not after it).  Boundaries
  * that break these rules give wrong masks but never an out-of-range access.
- * q [N, 1, S, H, d], k and v [N, 1, S, H_kv, d]; the rest as ra_ring_attn_fwd_gqa.
+ * q [N, 1, S, H, d], k and v [N, 1, S, H_kv, d] (with RA_FLAG_SEQ_ORDER the
+ * packed stream itself, [1, L, H, d] and [1, L, H_kv, d]); the rest as
+ * ra_ring_attn_fwd_gqa.
  */
 RA_API ra_status ra_ring_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
                                          float *lse, const int32_t *cu_seqlens, int n_seqs,

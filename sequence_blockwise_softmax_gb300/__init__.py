@@ -22,6 +22,7 @@ RA_CONTIGUOUS, RA_STRIPED, RA_ZIGZAG = range(3)
 RA_SEQ_TO_SHARDS, RA_SHARDS_TO_SEQ, RA_ULYSSES_SEQ_TO_HEAD, RA_ULYSSES_HEAD_TO_SEQ = range(4)
 RA_FLAG_STEPWISE = 1
 RA_FLAG_O_BF16 = 2
+RA_FLAG_SEQ_ORDER = 4
 RA_FLAG_INJECT_STALL = 0x80000000
 RA_WORKSPACE_MIN_BYTES = 256
 LAYOUTS = {"contiguous": RA_CONTIGUOUS, "striped": RA_STRIPED, "zigzag": RA_ZIGZAG}

@@ -232,7 +232,8 @@ ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const flo
 
 size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N, unsigned flags) {
     if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
-    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_INJECT_STALL)) return 0;
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_SEQ_ORDER | RA_FLAG_INJECT_STALL)) return 0;
+    if ((flags & RA_FLAG_SEQ_ORDER) && (flags & RA_FLAG_STEPWISE)) return 0;
     if (flags & RA_FLAG_STEPWISE) return stepwise_layout(B, L, H, d, (flags & RA_FLAG_O_BF16) != 0).total;
     return kHeader;
 }
@@ -245,16 +246,20 @@ ra_status ring_attn(const void *q, const void *k, const void *v, void *o, float 
                     int64_t L, int64_t H, int64_t H_kv, int d, int N, int layout, int causal,
                     float scale, unsigned flags, void *workspace, size_t workspace_bytes,
                     void *stream, const int *cu_seqlens = nullptr, int n_seqs = 0) {
-    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_INJECT_STALL))
+    if (flags & ~(RA_FLAG_STEPWISE | RA_FLAG_O_BF16 | RA_FLAG_SEQ_ORDER | RA_FLAG_INJECT_STALL))
         return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
     if ((flags & RA_FLAG_INJECT_STALL) && (flags & RA_FLAG_STEPWISE))
         return fail(RA_ERR_INVALID_ARG, "RA_FLAG_INJECT_STALL applies to the fused sweep only");
+    if ((flags & RA_FLAG_SEQ_ORDER) && (flags & RA_FLAG_STEPWISE))
+        return fail(RA_ERR_INVALID_ARG, "RA_FLAG_SEQ_ORDER applies to the fused sweep only");
     const bool o_bf16 = (flags & RA_FLAG_O_BF16) != 0;
     if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
     if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
     if (L % N) return fail(RA_ERR_SHAPE, "N must divide L");
     if (layout == RA_ZIGZAG && (L % (2 * (int64_t)N))) return fail(RA_ERR_SHAPE, "zigzag needs 2N | L");
     const int64_t S = L / N;
+    if ((flags & RA_FLAG_SEQ_ORDER) && layout == RA_ZIGZAG && (S / 2) % 128)
+        return fail(RA_ERR_UNSUPPORTED, "RA_FLAG_SEQ_ORDER with zigzag needs L / 2N to be a multiple of 128");
     ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
     if (st != RA_OK) return st;
     if (H > 0 && (st = check_kv_heads(H, H_kv)) != RA_OK) return st;
@@ -286,6 +291,7 @@ ra_status ring_attn(const void *q, const void *k, const void *v, void *o, float 
     a.ring = true;
     a.cu_seqlens = cu_seqlens;
     a.n_seqs = n_seqs;
+    a.seq_order = (flags & RA_FLAG_SEQ_ORDER) != 0;
     if (!(flags & RA_FLAG_STEPWISE)) {
         a.o = o;
         a.ring_step = -1;

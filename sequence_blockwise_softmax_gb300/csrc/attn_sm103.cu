@@ -67,7 +67,40 @@ struct AttnArgs {
     const int *cu_seqlens;  // packed sequences: n_seqs + 1 boundaries, or null
     int n_seqs;
     int bh_chunk;       // (batch, head) pairs whose units are interleaved heavy-first
+    int seq_order;      // q/k/v/o in sequence order [B, L, H, d], LSE [B, H, L] (ring mode)
 };
+
+// The outer TMA coordinates (after the column) of local rows [row, row + 128)
+// of rank `rank`'s shard of batch b.  Shard stacks [N or 1, B, S, H*d] are
+// addressed (row, b, rank).  In sequence order the layout is the addressing:
+// the host views [B, L, H*d] so that a shard's rows form one dimension --
+// contiguous {S, N, B} (position r*S + s), striped {N, S, B} (position s*N + r,
+// the row is the second coordinate), zigzag {C, 2N, B} with C = S/2 (rank r's
+// rows are chunk r, then chunk 2N-1-r; C is a multiple of 128, so a 128-row
+// tile never straddles the two).  Rows past a shard's end fall outside the
+// view: loads read zeros there and stores skip them.
+__device__ __forceinline__ void tile_coords(const AttnArgs &args, int rank, int b, int row, int &c1, int &c2,
+                                            int &c3) {
+    if (!args.seq_order) {
+        c1 = row;
+        c2 = b;
+        c3 = rank;
+    } else if (args.layout == RA_STRIPED) {
+        c1 = rank;
+        c2 = row;
+        c3 = b;
+    } else if (args.layout == RA_ZIGZAG) {
+        const int C = args.S >> 1;
+        const bool hi = row >= C;
+        c1 = hi ? row - C : row;
+        c2 = hi ? 2 * args.N - 1 - rank : rank;
+        c3 = b;
+    } else {
+        c1 = row;
+        c2 = rank;
+        c3 = b;
+    }
+}
 
 __device__ __forceinline__ void record_timeout(unsigned *status, volatile int *abort) {
     *abort = 1;
@@ -282,10 +315,13 @@ __global__ void __launch_bounds__(384, 1)
         const int xkv = (h / args.kv_group) * D;     // K/V columns of its key/value head
         if (lane == 0) {
             mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
-            for (int g = 0; g < 2; ++g)
+            for (int g = 0; g < 2; ++g) {
+                int c1, c2, c3;
+                tile_coords(args, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
                 for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kQ + g * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL),
-                                xh + 64 * c, row0 + 128 * g, zq);
+                    tma_load_4d(s_base + L::kQ + g * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL),
+                                xh + 64 * c, c1, c2, c3);
+            }
         }
         __syncwarp();
         // K and V tiles share a ring of three slots.  Load order K(0), K(1),
@@ -305,11 +341,12 @@ __global__ void __launch_bounds__(384, 1)
             const bool withhold = args.inject_stall && blockIdx.x == 0 && i == 1;
             if (lane == 0 && !withhold) {
                 const uint32_t dst = s_base + L::kRing + sl * L::kTile;
-                const int zkv = (ring ? wj * args.B : 0) + b, y = wtile * 128;
+                int c1, c2, c3;
+                tile_coords(args, ring ? wj : 0, b, wtile * 128, c1, c2, c3);
                 mbar_arrive_expect_tx(BAR(B_SLOTF + sl), L::kTile);
                 for (int c = 0; c < HALVES; ++c) {
-                    if (is_k) tma_load_3d(dst + c * L::kBox, &tmk, BAR(B_SLOTF + sl), xkv + 64 * c, y, zkv);
-                    else tma_load_3d(dst + c * L::kBox, &tmv, BAR(B_SLOTF + sl), xkv + 64 * c, y, zkv);
+                    if (is_k) tma_load_4d(dst + c * L::kBox, &tmk, BAR(B_SLOTF + sl), xkv + 64 * c, c1, c2, c3);
+                    else tma_load_4d(dst + c * L::kBox, &tmv, BAR(B_SLOTF + sl), xkv + 64 * c, c1, c2, c3);
                 }
             }
             __syncwarp();
@@ -943,12 +980,18 @@ __global__ void __launch_bounds__(384, 1)
         if (wq == 0 && lane == 0 && *abort_flag == 0) {
             // rows past the shard's end fall outside the tensor and are not written
 #pragma unroll
-            for (int bx = 0; bx < NBOX; ++bx) tma_store_3d(&tmo, box_addr(bx), h * D + bx * CPB, row0 + 128 * g, zq);
+            int c1, c2, c3;
+            tile_coords(args, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
+            for (int bx = 0; bx < NBOX; ++bx) tma_store_4d(&tmo, box_addr(bx), h * D + bx * CPB, c1, c2, c3);
             tma_store_commit();
             tma_store_wait_read();
         }
-        if (ok && a < S)
-            args.lse[((size_t)zq * H + h) * S + a] = l > 0.f ? (m_ref + lg2(l)) * 0.6931471805599453f : -INFINITY;
+        if (ok && a < S) {
+            // shard stacks: [N or 1, B, H, S]; sequence order: [B, H, L] at the row's position
+            const size_t at = args.seq_order ? ((size_t)b * H + h) * ((size_t)N * S) + (size_t)my_pos
+                                             : ((size_t)zq * H + h) * S + a;
+            args.lse[at] = l > 0.f ? (m_ref + lg2(l)) * 0.6931471805599453f : -INFINITY;
+        }
     }
 
     // ---- teardown: every role is here, all tensor-core work has finished
@@ -982,16 +1025,39 @@ static EncodeTiledFn get_encode_fn() {
 // [Z, S, H*d] bf16 (or fp32) viewed as a 3-D tensor, boxes of 128 rows x
 // 128 bytes (64 bf16 or 32 fp32 columns) with the 128-byte swizzle the MMA
 // descriptors and the O staging expect.
-static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d,
+// The 4-D view of a [..., heads * d] tensor that tile_coords addresses: the
+// columns, then the three outer dimensions of the launch's addressing mode,
+// with a box of 128 bytes of columns by 128 rows (rows are dimension 1, or 2
+// for sequence-order striped) and the 128-byte swizzle the operand
+// descriptors expect.
+static bool make_map(CUtensorMap *map, const void *base, const AttnLaunch &a, int64_t heads, int d,
                      bool f32 = false) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t esz = f32 ? 4 : 2;
-    cuuint64_t dims[3] = {(cuuint64_t)(H * d), (cuuint64_t)S, (cuuint64_t)Z};
-    cuuint64_t strides[2] = {(cuuint64_t)(H * d) * esz, (cuuint64_t)(S * H * d) * esz};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    const int64_t cols = heads * d, S = a.S, B = a.B, N = a.N;
+    int64_t n[3], st[3];   // outer extents and their element strides
+    int row_dim = 1;
+    if (!a.seq_order) {                      // [N or 1, B, S, cols]
+        n[0] = S, n[1] = B, n[2] = a.ring ? N : 1;
+        st[0] = cols, st[1] = S * cols, st[2] = B * S * cols;
+    } else if (a.layout == RA_STRIPED) {     // [B, S, N, cols]: position s*N + r
+        n[0] = N, n[1] = S, n[2] = B;
+        st[0] = cols, st[1] = N * cols, st[2] = N * S * cols;
+        row_dim = 2;
+    } else if (a.layout == RA_ZIGZAG) {      // [B, 2N, C, cols]: position chunk*C + c
+        const int64_t C = S / 2;
+        n[0] = C, n[1] = 2 * N, n[2] = B;
+        st[0] = cols, st[1] = C * cols, st[2] = N * S * cols;
+    } else {                                 // [B, N, S, cols]: position r*S + s
+        n[0] = S, n[1] = N, n[2] = B;
+        st[0] = cols, st[1] = S * cols, st[2] = N * S * cols;
+    }
+    cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)n[0], (cuuint64_t)n[1], (cuuint64_t)n[2]};
+    cuuint64_t strides[3] = {(cuuint64_t)st[0] * esz, (cuuint64_t)st[1] * esz, (cuuint64_t)st[2] * esz};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / esz), row_dim == 1 ? 128u : 1u, row_dim == 2 ? 128u : 1u, 1u};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -999,12 +1065,12 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, i
 }
 
 template <int D, bool F32, bool SKIP>
-static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t Zq, int64_t Zkv,
-                          int64_t grid, cudaStream_t stream, const char **err) {
+static ra_status launch_t(const AttnLaunch &a, const AttnArgs &args, int64_t grid, cudaStream_t stream,
+                          const char **err) {
     CUtensorMap mq, mk, mv, mo;
     const int64_t Hkv = a.H_kv > 0 ? a.H_kv : a.H;
-    if (!make_map(&mq, a.q, Zq, a.S, a.H, D) || !make_map(&mk, a.k, Zkv, a.S, Hkv, D) ||
-        !make_map(&mv, a.v, Zkv, a.S, Hkv, D) || !make_map(&mo, a.o, Zq, a.S, a.H, D, F32)) {
+    if (!make_map(&mq, a.q, a, a.H, D) || !make_map(&mk, a.k, a, Hkv, D) || !make_map(&mv, a.v, a, Hkv, D) ||
+        !make_map(&mo, a.o, a, a.H, D, F32)) {
         *err = "cuTensorMapEncodeTiled failed for the q/k/v/o tensor maps";
         return RA_ERR_CUDA;
     }
@@ -1049,8 +1115,7 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     // keys + values one query head sweeps, shared by the heads of a GQA group;
     // a chunk holds about 48 MB of them by default (L2 holds 129 MB)
     args.bh_chunk = chunk_pairs(2 * (a.ring ? a.N : 1) * a.S * a.d * 2 / args.kv_group, a.B * a.H);
-    const int64_t Zq = a.ring ? a.N * a.B : a.B;
-    const int64_t Zkv = Zq;
+    args.seq_order = a.seq_order ? 1 : 0;
     const int64_t grid = (int64_t)args.num_q_ranks * args.n_units_seq * a.B * a.H;
     if (grid == 0) return RA_OK;
     if (grid > 0x7fffffffLL) {
@@ -1064,13 +1129,13 @@ ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char 
     // packed sequences too).
     const bool skip = a.d == 128 && a.cu_seqlens != nullptr && a.layout == RA_STRIPED;
     if (skip)
-        return a.out_f32 ? launch_t<128, true, true>(a, args, Zq, Zkv, grid, stream, err)
-                         : launch_t<128, false, true>(a, args, Zq, Zkv, grid, stream, err);
+        return a.out_f32 ? launch_t<128, true, true>(a, args, grid, stream, err)
+                         : launch_t<128, false, true>(a, args, grid, stream, err);
     if (a.d == 128)
-        return a.out_f32 ? launch_t<128, true, false>(a, args, Zq, Zkv, grid, stream, err)
-                         : launch_t<128, false, false>(a, args, Zq, Zkv, grid, stream, err);
-    return a.out_f32 ? launch_t<64, true, false>(a, args, Zq, Zkv, grid, stream, err)
-                     : launch_t<64, false, false>(a, args, Zq, Zkv, grid, stream, err);
+        return a.out_f32 ? launch_t<128, true, false>(a, args, grid, stream, err)
+                         : launch_t<128, false, false>(a, args, grid, stream, err);
+    return a.out_f32 ? launch_t<64, true, false>(a, args, grid, stream, err)
+                     : launch_t<64, false, false>(a, args, grid, stream, err);
 }
 
 }  // namespace ra

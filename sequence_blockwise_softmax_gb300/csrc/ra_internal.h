@@ -34,6 +34,7 @@ struct AttnLaunch {
     bool inject_stall;    // test hook, see RA_FLAG_INJECT_STALL
     const int *cu_seqlens;  // packed sequences (device, n_seqs + 1 boundaries), or null
     int n_seqs;
+    bool seq_order;       // ring mode: q/k/v/o [B, L, H, d] and LSE [B, H, L] in sequence order
 };
 
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);

@@ -58,6 +58,8 @@ def _ring(ralib, **kw):
     (dict(o=FAKE + 8), 4),                     # misaligned
     (dict(wsb=16), 1),                         # workspace too small
     (dict(flags=1, wsb=256), 1),               # stepwise needs the big workspace
+    (dict(flags=5), 1),                        # sequence order is fused-sweep only
+    (dict(flags=4, layout=2, L=1280), 3),      # sequence-order zigzag: chunk 160 is not a multiple of 128
 ])
 def test_ring_rejects_bad_arguments(ralib, kw, status):
     assert _ring(ralib, **kw) == status
@@ -126,7 +128,9 @@ def test_workspace_sizes(ralib):
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 1) == 256 + n * 4 + 1024 * 2 * 4
     # stepwise, bf16 O: an fp32 accumulator as well
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 3) == 256 + 2 * n * 4 + 1024 * 2 * 4
-    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 4) == 0
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 4) == 256    # sequence order
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 5) == 0      # ... not stepwise
+    assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 128, 4, 8) == 0      # unknown flag
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 96, 4, 0) == 0
 
 
