@@ -284,20 +284,35 @@ class Workload:
             raise ValueError("the backward bench runs plain ring layouts")
         self.step()
         self.do_seq = make_dout(B, L, H, d).to(self.dev)
+        self.bws = ra.new_workspace(ra.ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N), device=self.dev)
+        self.flops = 2.0 * self.flops
+        self.dq_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=self.dev)
+        self.dk_seq = torch.empty((B, L, self.Hkv, d), dtype=torch.float32, device=self.dev)
+        self.dv_seq = torch.empty_like(self.dk_seq)
+        if self.seq_order:
+            # token order: D = rowsum(dO * O), the dK/dV pass and the dQ pass, no permutes
+            self.launches = 3
+            return
         self.do_shard = torch.empty_like(self.shard[0])
         S = L // N
         self.dq = torch.empty((N, B, S, H, d), dtype=torch.float32, device=self.dev)
         self.dk = torch.empty((N, B, S, self.Hkv, d), dtype=torch.float32, device=self.dev)
         self.dv = torch.empty_like(self.dk)
-        self.dq_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=self.dev)
-        self.dk_seq = torch.empty((B, L, self.Hkv, d), dtype=torch.float32, device=self.dev)
-        self.dv_seq = torch.empty_like(self.dk_seq)
-        self.bws = ra.new_workspace(ra.ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N), device=self.dev)
-        self.flops = 2.0 * self.flops
         self.launches = 1 + 3 + 3
 
     def step_bwd(self, time_attention=False):
         ra, B, L, H, d, N = self.ra, self.B, self.L, self.H, self.d, self.N
+        if self.seq_order:
+            if time_attention:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            ra.ra_ring_attn_bwd(*self.seq, self.o_seq, self.do_seq, self.lse_seq, self.dq_seq, self.dk_seq,
+                                self.dv_seq, B, L, H, self.Hkv, d, N, self.layout, self.causal, workspace=self.bws,
+                                flags=ra.RA_FLAG_SEQ_ORDER)
+            if time_attention:
+                e1.record()
+                self.attn_events.append((e0, e1))
+            return
         ra.ra_shard_permute(self.do_seq, self.do_shard, ra.RA_SEQ_TO_SHARDS, self.layout, B, L, H, d, N)
         if time_attention:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -578,7 +593,7 @@ def main():
     layout = args.layout or w["layouts"][0]
     shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
     wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise, kv_heads=args.kv_heads,
-                  varlen=args.varlen, seq_order=not (args.explicit_permutes or args.backward))
+                  varlen=args.varlen, seq_order=not args.explicit_permutes)
 
     step = wl.step
     if args.backward:

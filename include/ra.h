@@ -271,14 +271,19 @@ RA_API ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void *k,
  * output [N, B, S, H, d]; dout: bf16 gradient of O, like q; lse: fp32
  * [N, B, H, S] from the forward.  dq: fp32 like q; dk, dv: fp32 like k.
  * cu_seqlens / n_seqs: packed sequences as in ra_ring_attn_fwd_varlen (B = 1),
- * or NULL / 0.  d in {64, 128}; workspace: ra_ring_attn_bwd_workspace_bytes()
- * bytes (status word and D), zero-filled before its first use.
+ * or NULL / 0.  d in {64, 128}.  flags: 0 or RA_FLAG_SEQ_ORDER, with which
+ * every tensor is in token order as in the forward of that flag (q, dout, o,
+ * dq [B, L, H, d]; k, v, dk, dv [B, L, H_kv, d]; lse [B, H, L]), with the
+ * same zigzag condition; the results equal the shard-stack call's, bit for
+ * bit, in token order.  workspace: ra_ring_attn_bwd_workspace_bytes() bytes
+ * (status word, D, and in token order a stack-order copy of lse),
+ * zero-filled before its first use.
  */
 RA_API ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const float *o,
                                   const void *dout, const float *lse, float *dq, float *dk,
                                   float *dv, const int32_t *cu_seqlens, int n_seqs, int64_t B,
                                   int64_t L, int64_t H, int64_t H_kv, int d, int N, int layout,
-                                  int causal, float scale, void *workspace,
+                                  int causal, float scale, unsigned flags, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
 /* Workspace bytes ra_ring_attn_bwd needs (0 on bad arguments). */

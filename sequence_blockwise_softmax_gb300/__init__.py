@@ -48,7 +48,7 @@ SIGNATURES = {
     "ra_ring_attn_fwd_stepwise_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I,
                                                _F, _P]),
     "ra_ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I64, _I, _I,
-                              _I, _I, _F, _P, _SZ, _P]),
+                              _I, _I, _F, _U, _P, _SZ, _P]),
     "ra_ring_attn_bwd_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "ra_check_status": (_I, [_P, _P]),
     "ra_last_error": (ctypes.c_char_p, []),
@@ -223,7 +223,7 @@ def ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N):
 
 
 def ra_ring_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, L, H, H_kv, d, N, layout, causal,
-                     scale=0.0, cu_seqlens=None, workspace=None, stream=None):
+                     scale=0.0, cu_seqlens=None, workspace=None, stream=None, flags=0):
     """Gradients of the ring attention; o fp32, dout bf16; dq / dk / dv fp32 outputs."""
     for t in (q, k, v, dout):
         assert t.dtype == torch.bfloat16
@@ -236,7 +236,7 @@ def ra_ring_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, L, H, H_kv, d, N, lay
     _check(lib().ra_ring_attn_bwd(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(o, "o"),
                                   _ptr(dout, "dout"), _ptr(lse, "lse"), _ptr(dq, "dq"), _ptr(dk, "dk"),
                                   _ptr(dv, "dv"), _ptr(cu_seqlens, "cu_seqlens"), n_seqs, B, L, H, H_kv,
-                                  d, N, _layout(layout), int(bool(causal)), float(scale),
+                                  d, N, _layout(layout), int(bool(causal)), float(scale), int(flags),
                                   _ptr(workspace, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 

@@ -359,19 +359,23 @@ ra_status ra_ring_attn_fwd_varlen(const void *q, const void *k, const void *v, v
 
 size_t ra_ring_attn_bwd_workspace_bytes(int64_t B, int64_t L, int64_t H, int d, int N) {
     if (B < 0 || L < 0 || H < 0 || N < 1 || (d != 64 && d != 128)) return 0;
-    return kHeader + round256((size_t)B * (size_t)L * (size_t)H * 4);
+    // the status word, D, and the stack-order copy of lse a token-order call makes
+    return kHeader + 2 * round256((size_t)B * (size_t)L * (size_t)H * 4);
 }
 
 ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const float *o,
                            const void *dout, const float *lse, float *dq, float *dk, float *dv,
                            const int32_t *cu_seqlens, int n_seqs, int64_t B, int64_t L, int64_t H,
                            int64_t H_kv, int d, int N, int layout, int causal, float scale,
-                           void *workspace, size_t workspace_bytes, void *stream) {
+                           unsigned flags, void *workspace, size_t workspace_bytes, void *stream) {
+    if (flags & ~RA_FLAG_SEQ_ORDER) return fail(RA_ERR_INVALID_ARG, "unknown flag bits");
     if (N < 1) return fail(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
     if (L < 0) return fail(RA_ERR_SHAPE, "L must be non-negative");
     if (L % N) return fail(RA_ERR_SHAPE, "N must divide L");
     if (layout == RA_ZIGZAG && (L % (2 * (int64_t)N))) return fail(RA_ERR_SHAPE, "zigzag needs 2N | L");
     const int64_t S = L / N;
+    if ((flags & RA_FLAG_SEQ_ORDER) && layout == RA_ZIGZAG && (S / 2) % 128)
+        return fail(RA_ERR_UNSUPPORTED, "RA_FLAG_SEQ_ORDER with zigzag needs L / 2N to be a multiple of 128");
     ra_status st = check_attn_common(B, S, H, d, N, layout, scale);
     if (st != RA_OK) return st;
     if (H > 0 && (st = check_kv_heads(H, H_kv)) != RA_OK) return st;
@@ -397,6 +401,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const fl
     a.o = o;
     a.lse = lse;
     a.dvec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeader);
+    a.lse_stack = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeader +
+                                            round256((size_t)B * (size_t)L * (size_t)H * 4));
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -407,6 +413,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, const fl
     a.S = S;
     a.H = H;
     a.H_kv = H_kv;
+    a.seq_order = (flags & RA_FLAG_SEQ_ORDER) != 0;
     a.d = d;
     a.N = N;
     a.layout = layout;

@@ -46,11 +46,15 @@
 
 namespace ra {
 
+// lse and dvec are [Z, H, S] (Z = N * B) in both forms (in token order lse
+// is the stack-order copy bwd_dot makes).  dq [Z, S, H, d] and dk, dv
+// [Z, S, H_kv, d] in shard stacks; in token order (seq_order) dq [B, L, H, d]
+// and dk, dv [B, L, H_kv, d], a row at its token position.
 struct BwdArgs {
-    const float *lse;       // [Z, H, S] natural log (forward output)
-    const float *dvec;      // [Z, H, S] D = rowsum(dO * O)
-    float *dq;              // [Z, S, H, d]
-    float *dk, *dv;         // [Z, S, H_kv, d]
+    const float *lse;       // natural log (forward output)
+    const float *dvec;      // D = rowsum(dO * O)
+    float *dq;
+    float *dk, *dv;
     unsigned *status;
     const int *cu_seqlens;
     int n_seqs;
@@ -59,6 +63,7 @@ struct BwdArgs {
     int n_tiles_seq;        // ceil(S / 128)
     int bh_chunk_q;         // (batch, head) pairs interleaved heavy-first in the dQ pass
     int bh_chunk_kv;        // (batch, key/value head) pairs, the same in the dK/dV pass
+    int seq_order;          // token-order tensors (the layout is the tiles' addresses)
 };
 
 // Tile decode shared by both passes: (batch, head) pairs are taken in chunks
@@ -166,25 +171,38 @@ __device__ __forceinline__ void store_row32(float *dst, const uint32_t (&r)[32],
 }
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
+// One warp per row (z, s, h) of the [Z, S, H] shard stacks, Z = N * B:
+// D[(z * H + h) * S + s] = dO . O.  In token order the row's O and dO are read
+// at its token position, and its LSE ([B, H, L]) is copied to the same
+// stack-order index of lse_stack, so that both passes read D and LSE of a
+// tile's rows as one contiguous run.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_dot_kernel(const uint16_t *dout, const float *o,
-                                                      float *dvec, int64_t rows, int H, int64_t S) {
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const uint16_t *dout, const float *o, float *dvec,
+                                                      int64_t rows, int H, int64_t S, int seq_order, int layout,
+                                                      int N, int B, const float *lse_tok, float *lse_stack) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     constexpr int PER = D / 32;   // elements per lane
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-        const uint16_t *dp = dout + r * D + lane * PER;
-        const float *op = o + r * D + lane * PER;
+        const int64_t h = r % H, zs = r / H;
+        const int64_t s = zs % S, z = zs / S;
+        int64_t src = r, at_tok = 0;
+        if (seq_order) {
+            const int rank = (int)(z / B), b = (int)(z % B);
+            const int64_t p = token_pos(layout, rank, s, N, S);
+            src = ((int64_t)b * N * S + p) * H + h;
+            at_tok = ((int64_t)b * H + h) * N * S + p;
+        }
+        const uint16_t *dp = dout + src * D + lane * PER;
+        const float *op = o + src * D + lane * PER;
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < PER; ++e) acc += __uint_as_float((uint32_t)dp[e] << 16) * op[e];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-            // row r = (z * S + s) * H + h  ->  D index (z * H + h) * S + s
-            const int64_t h = r % H, zs = r / H;
-            const int64_t s = zs % S, z = zs / S;
             dvec[(z * H + h) * S + s] = acc;
+            if (seq_order) lse_stack[(z * H + h) * S + s] = lse_tok[at_tok];
         }
     }
 }
@@ -308,9 +326,11 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         if (lane == 0) {
             mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
+            int c1, c2, c3;
+            tile_coords(args.seq_order, args.layout, S, N, qi, b, row0, c1, c2, c3);
             for (int c = 0; c < HALVES; ++c) {
-                tma_load_3d(s_base + L::kQ + c * L::kBox, &tmq, BAR(B_QFULL), h * D + 64 * c, row0, zq);
-                tma_load_3d(s_base + L::kDO + c * L::kBox, &tmdo, BAR(B_QFULL), h * D + 64 * c, row0, zq);
+                tma_load_4d(s_base + L::kQ + c * L::kBox, &tmq, BAR(B_QFULL), h * D + 64 * c, c1, c2, c3);
+                tma_load_4d(s_base + L::kDO + c * L::kBox, &tmdo, BAR(B_QFULL), h * D + 64 * c, c1, c2, c3);
             }
         }
         __syncwarp();
@@ -318,13 +338,14 @@ __global__ void __launch_bounds__(384, 1)
         w.start_step();
         for (; w.valid(); w.next(), ++t) {
             const int sk = t % NK, sv = t % NV;
-            const int zkv = w.j * args.B + b, y = w.tile * 128;
+            int k1, k2, k3;
+            tile_coords(args.seq_order, args.layout, S, N, w.j, b, w.tile * 128, k1, k2, k3);
             if (t >= NK && !(ok = warp_wait(BAR(B_KEMPTY + sk), ((t / NK) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_KFULL + sk), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kK + sk * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + sk),
-                                hk * D + 64 * c, y, zkv);
+                    tma_load_4d(s_base + L::kK + sk * L::kTile + c * L::kBox, &tmk, BAR(B_KFULL + sk),
+                                hk * D + 64 * c, k1, k2, k3);
             }
             __syncwarp();
             k_issued = t + 1;
@@ -332,8 +353,8 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_VFULL + sv), L::kTile);
                 for (int c = 0; c < HALVES; ++c)
-                    tma_load_3d(s_base + L::kV + sv * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + sv),
-                                hk * D + 64 * c, y, zkv);
+                    tma_load_4d(s_base + L::kV + sv * L::kTile + c * L::kBox, &tmv, BAR(B_VFULL + sv),
+                                hk * D + 64 * c, k1, k2, k3);
             }
             __syncwarp();
             v_issued = t + 1;
@@ -512,7 +533,8 @@ __global__ void __launch_bounds__(384, 1)
             // tensor-memory loads are warp-wide; only the stores depend on the row.
             // Each half writes half of the d columns.
             if (ok) {
-                float *dst = args.dq + (((size_t)zq * S + a_c) * H + h) * D;
+                float *dst = args.dq + ((args.seq_order ? (size_t)b * total + (size_t)my_pos
+                                                        : (size_t)zq * S + a_c) * H + h) * D;
 #pragma unroll
                 for (int q = hh * (D / 64); q < (hh + 1) * (D / 64); ++q) {
                     uint32_t v[32];
@@ -688,9 +710,11 @@ __global__ void __launch_bounds__(384, 1)
         int t = 0, issued = 0;
         if (lane == 0) {
             mbar_arrive_expect_tx(BAR(B_KVFULL), 2 * L::kTile);
+            int c1, c2, c3;
+            tile_coords(args.seq_order, args.layout, S, N, kj, b, c0, c1, c2, c3);
             for (int c = 0; c < HALVES; ++c) {
-                tma_load_3d(s_base + L::kK + c * L::kBox, &tmk, BAR(B_KVFULL), hk * D + 64 * c, c0, zk);
-                tma_load_3d(s_base + L::kV + c * L::kBox, &tmv, BAR(B_KVFULL), hk * D + 64 * c, c0, zk);
+                tma_load_4d(s_base + L::kK + c * L::kBox, &tmk, BAR(B_KVFULL), hk * D + 64 * c, c1, c2, c3);
+                tma_load_4d(s_base + L::kV + c * L::kBox, &tmv, BAR(B_KVFULL), hk * D + 64 * c, c1, c2, c3);
             }
         }
         __syncwarp();
@@ -699,10 +723,10 @@ __global__ void __launch_bounds__(384, 1)
         for (; w.valid(); w.next(), ++t) {
             const int st = t % NS;
             const int h = hk * group + w.head;
-            const int zq = w.i * args.B + b, y = w.tile * 128;
+            const int y = w.tile * 128;
             // -lse*log2(e) and D of the 128 query rows (0 past the shard's end),
             // read before the stage wait so their latency overlaps it
-            const size_t base = ((size_t)zq * H + h) * S;
+            const size_t base = ((size_t)(w.i * args.B + b) * H + h) * S;
             float nl[4], dd[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -711,14 +735,16 @@ __global__ void __launch_bounds__(384, 1)
                 nl[e] = lv > -INFINITY ? lv * -1.4426950408889634f : 0.f;
                 dd[e] = row < S ? args.dvec[base + row] : 0.f;
             }
+            int c1, c2, c3;
+            tile_coords(args.seq_order, args.layout, S, N, w.i, b, y, c1, c2, c3);
             if (t >= NS && !(ok = warp_wait(BAR(B_QEMPTY + st), ((t / NS) - 1) & 1, abort_flag))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(B_QFULL + st), 2 * L::kTile);
                 for (int c = 0; c < HALVES; ++c) {
-                    tma_load_3d(s_base + L::kQ + st * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL + st),
-                                h * D + 64 * c, y, zq);
-                    tma_load_3d(s_base + L::kDO + st * L::kTile + c * L::kBox, &tmdo, BAR(B_QFULL + st),
-                                h * D + 64 * c, y, zq);
+                    tma_load_4d(s_base + L::kQ + st * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL + st),
+                                h * D + 64 * c, c1, c2, c3);
+                    tma_load_4d(s_base + L::kDO + st * L::kTile + c * L::kBox, &tmdo, BAR(B_QFULL + st),
+                                h * D + 64 * c, c1, c2, c3);
                 }
             }
             float *vec = reinterpret_cast<float *>(smem + L::kVec + st * 1024);
@@ -942,7 +968,8 @@ __global__ void __launch_bounds__(384, 1)
             // tensor-memory loads are warp-wide; only the stores depend on the row.
             // Each half writes half of the d columns.
             if (ok) {
-                const size_t row = (((size_t)zk * S + kk_c) * Hkv + hk) * D;
+                const size_t row = ((args.seq_order ? (size_t)b * total + (size_t)kpos
+                                                    : (size_t)zk * S + kk_c) * Hkv + hk) * D;
 #pragma unroll
                 for (int q = hh * (D / 64); q < (hh + 1) * (D / 64); ++q) {
                     uint32_t v[32];
@@ -990,28 +1017,31 @@ static BwdEncodeFn bwd_encode_fn() {
     return fn;
 }
 
-static bool bwd_map(CUtensorMap *map, const void *base, int64_t Z, int64_t S, int64_t H, int d) {
+// The 4-D view tile_view describes (shard stacks or token order), bf16, with
+// a box of 64 columns by 128 rows in the 128-byte swizzle.
+static bool bwd_map(CUtensorMap *map, const void *base, const BwdLaunch &a, int64_t heads, int d) {
     BwdEncodeFn enc = bwd_encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)(H * d), (cuuint64_t)S, (cuuint64_t)Z};
-    cuuint64_t strides[2] = {(cuuint64_t)(H * d * 2), (cuuint64_t)(S * H * d * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const TileView tv = tile_view(a.seq_order, a.layout, a.S, a.B, a.N, a.N, heads * d);
+    cuuint64_t dims[4] = {(cuuint64_t)(heads * d), (cuuint64_t)tv.n[0], (cuuint64_t)tv.n[1], (cuuint64_t)tv.n[2]};
+    cuuint64_t strides[3] = {(cuuint64_t)tv.st[0] * 2, (cuuint64_t)tv.st[1] * 2, (cuuint64_t)tv.st[2] * 2};
+    cuuint32_t box[4] = {64, tv.row_dim == 0 ? 128u : 1u, tv.row_dim == 1 ? 128u : 1u, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D>
 static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t stream, const char **err) {
     const int64_t Z = (int64_t)a.N * a.B;
     CUtensorMap mq, mk, mv, mdo;
-    if (!bwd_map(&mq, a.q, Z, a.S, a.H, D) || !bwd_map(&mk, a.k, Z, a.S, a.H_kv, D) ||
-        !bwd_map(&mv, a.v, Z, a.S, a.H_kv, D) || !bwd_map(&mdo, a.dout, Z, a.S, a.H, D)) {
+    if (!bwd_map(&mq, a.q, a, a.H, D) || !bwd_map(&mk, a.k, a, a.H_kv, D) || !bwd_map(&mv, a.v, a, a.H_kv, D) ||
+        !bwd_map(&mdo, a.dout, a, a.H, D)) {
         *err = "cuTensorMapEncodeTiled failed for the backward tensor maps";
         return RA_ERR_CUDA;
     }
-    // D = rowsum(dO * O)
+    // D = rowsum(dO * O) (and, in token order, the stack-order LSE copy)
     {
         const int64_t rows = Z * a.S * a.H;
         int dev = 0, sms = 148;
@@ -1020,7 +1050,8 @@ static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t str
         int64_t blocks = (rows + 7) / 8;
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
         bwd_dot_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(a.dout), a.o,
-                                                                 a.dvec, rows, (int)a.H, a.S);
+                                                                 a.dvec, rows, (int)a.H, a.S, a.seq_order ? 1 : 0,
+                                                                 a.layout, a.N, (int)a.B, a.lse, a.lse_stack);
     }
     auto kq = attn_bwd_dq_kernel<D>;
     auto kkv = attn_bwd_dkv_kernel<D>;
@@ -1049,7 +1080,7 @@ static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t str
 
 ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const char **err) {
     BwdArgs args;
-    args.lse = a.lse;
+    args.lse = a.seq_order ? a.lse_stack : a.lse;
     args.dvec = a.dvec;
     args.dq = a.dq;
     args.dk = a.dk;
@@ -1067,6 +1098,7 @@ ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const ch
     args.scale = a.scale > 0.f ? a.scale : 1.0f / std::sqrt((float)a.d);
     args.scale_log2 = args.scale * 1.4426950408889634f;
     args.n_tiles_seq = (int)((a.S + 127) / 128);
+    args.seq_order = a.seq_order ? 1 : 0;
     if ((int64_t)a.N * a.B * a.S * a.H == 0) return RA_OK;
     {
         // bytes a tile's sweep streams per (batch, head) pair: keys + values

@@ -70,38 +70,6 @@ struct AttnArgs {
     int seq_order;      // q/k/v/o in sequence order [B, L, H, d], LSE [B, H, L] (ring mode)
 };
 
-// The outer TMA coordinates (after the column) of local rows [row, row + 128)
-// of rank `rank`'s shard of batch b.  Shard stacks [N or 1, B, S, H*d] are
-// addressed (row, b, rank).  In sequence order the layout is the addressing:
-// the host views [B, L, H*d] so that a shard's rows form one dimension --
-// contiguous {S, N, B} (position r*S + s), striped {N, S, B} (position s*N + r,
-// the row is the second coordinate), zigzag {C, 2N, B} with C = S/2 (rank r's
-// rows are chunk r, then chunk 2N-1-r; C is a multiple of 128, so a 128-row
-// tile never straddles the two).  Rows past a shard's end fall outside the
-// view: loads read zeros there and stores skip them.
-__device__ __forceinline__ void tile_coords(const AttnArgs &args, int rank, int b, int row, int &c1, int &c2,
-                                            int &c3) {
-    if (!args.seq_order) {
-        c1 = row;
-        c2 = b;
-        c3 = rank;
-    } else if (args.layout == RA_STRIPED) {
-        c1 = rank;
-        c2 = row;
-        c3 = b;
-    } else if (args.layout == RA_ZIGZAG) {
-        const int C = args.S >> 1;
-        const bool hi = row >= C;
-        c1 = hi ? row - C : row;
-        c2 = hi ? 2 * args.N - 1 - rank : rank;
-        c3 = b;
-    } else {
-        c1 = row;
-        c2 = rank;
-        c3 = b;
-    }
-}
-
 __device__ __forceinline__ void record_timeout(unsigned *status, volatile int *abort) {
     *abort = 1;
     atomicOr(status, RA_DEV_TIMEOUT_BIT);
@@ -317,7 +285,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive_expect_tx(BAR(B_QFULL), 2 * L::kTile);
             for (int g = 0; g < 2; ++g) {
                 int c1, c2, c3;
-                tile_coords(args, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
+                tile_coords(args.seq_order, args.layout, args.S, args.N, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
                 for (int c = 0; c < HALVES; ++c)
                     tma_load_4d(s_base + L::kQ + g * L::kTile + c * L::kBox, &tmq, BAR(B_QFULL),
                                 xh + 64 * c, c1, c2, c3);
@@ -342,7 +310,7 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0 && !withhold) {
                 const uint32_t dst = s_base + L::kRing + sl * L::kTile;
                 int c1, c2, c3;
-                tile_coords(args, ring ? wj : 0, b, wtile * 128, c1, c2, c3);
+                tile_coords(args.seq_order, args.layout, args.S, args.N, ring ? wj : 0, b, wtile * 128, c1, c2, c3);
                 mbar_arrive_expect_tx(BAR(B_SLOTF + sl), L::kTile);
                 for (int c = 0; c < HALVES; ++c) {
                     if (is_k) tma_load_4d(dst + c * L::kBox, &tmk, BAR(B_SLOTF + sl), xkv + 64 * c, c1, c2, c3);
@@ -981,7 +949,7 @@ __global__ void __launch_bounds__(384, 1)
             // rows past the shard's end fall outside the tensor and are not written
 #pragma unroll
             int c1, c2, c3;
-            tile_coords(args, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
+            tile_coords(args.seq_order, args.layout, args.S, args.N, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
             for (int bx = 0; bx < NBOX; ++bx) tma_store_4d(&tmo, box_addr(bx), h * D + bx * CPB, c1, c2, c3);
             tma_store_commit();
             tma_store_wait_read();
@@ -1025,37 +993,18 @@ static EncodeTiledFn get_encode_fn() {
 // [Z, S, H*d] bf16 (or fp32) viewed as a 3-D tensor, boxes of 128 rows x
 // 128 bytes (64 bf16 or 32 fp32 columns) with the 128-byte swizzle the MMA
 // descriptors and the O staging expect.
-// The 4-D view of a [..., heads * d] tensor that tile_coords addresses: the
-// columns, then the three outer dimensions of the launch's addressing mode,
-// with a box of 128 bytes of columns by 128 rows (rows are dimension 1, or 2
-// for sequence-order striped) and the 128-byte swizzle the operand
-// descriptors expect.
+// The 4-D view tile_view describes, for a [..., heads * d] tensor of the
+// launch, with a box of 128 bytes of columns by 128 rows and the 128-byte
+// swizzle the operand descriptors expect.
 static bool make_map(CUtensorMap *map, const void *base, const AttnLaunch &a, int64_t heads, int d,
                      bool f32 = false) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t esz = f32 ? 4 : 2;
-    const int64_t cols = heads * d, S = a.S, B = a.B, N = a.N;
-    int64_t n[3], st[3];   // outer extents and their element strides
-    int row_dim = 1;
-    if (!a.seq_order) {                      // [N or 1, B, S, cols]
-        n[0] = S, n[1] = B, n[2] = a.ring ? N : 1;
-        st[0] = cols, st[1] = S * cols, st[2] = B * S * cols;
-    } else if (a.layout == RA_STRIPED) {     // [B, S, N, cols]: position s*N + r
-        n[0] = N, n[1] = S, n[2] = B;
-        st[0] = cols, st[1] = N * cols, st[2] = N * S * cols;
-        row_dim = 2;
-    } else if (a.layout == RA_ZIGZAG) {      // [B, 2N, C, cols]: position chunk*C + c
-        const int64_t C = S / 2;
-        n[0] = C, n[1] = 2 * N, n[2] = B;
-        st[0] = cols, st[1] = C * cols, st[2] = N * S * cols;
-    } else {                                 // [B, N, S, cols]: position r*S + s
-        n[0] = S, n[1] = N, n[2] = B;
-        st[0] = cols, st[1] = S * cols, st[2] = N * S * cols;
-    }
-    cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)n[0], (cuuint64_t)n[1], (cuuint64_t)n[2]};
-    cuuint64_t strides[3] = {(cuuint64_t)st[0] * esz, (cuuint64_t)st[1] * esz, (cuuint64_t)st[2] * esz};
-    cuuint32_t box[4] = {(cuuint32_t)(128 / esz), row_dim == 1 ? 128u : 1u, row_dim == 2 ? 128u : 1u, 1u};
+    const TileView tv = tile_view(a.seq_order, a.layout, a.S, a.B, a.N, a.ring ? a.N : 1, heads * d);
+    cuuint64_t dims[4] = {(cuuint64_t)(heads * d), (cuuint64_t)tv.n[0], (cuuint64_t)tv.n[1], (cuuint64_t)tv.n[2]};
+    cuuint64_t strides[3] = {(cuuint64_t)tv.st[0] * esz, (cuuint64_t)tv.st[1] * esz, (cuuint64_t)tv.st[2] * esz};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / esz), tv.row_dim == 0 ? 128u : 1u, tv.row_dim == 1 ? 128u : 1u, 1u};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -66,6 +66,8 @@ struct BwdLaunch {
     int64_t B, S, H, H_kv;
     int d, N, layout, causal;
     float scale;
+    bool seq_order;       // q/k/v/o/dout/dq/dk/dv [B, L, ., d] and lse [B, H, L] in token order
+    float *lse_stack;     // token order: workspace for the [N, B, H, S] copy of lse
 };
 
 ra_status launch_attention_bwd(const BwdLaunch &a, cudaStream_t stream, const char **err);
@@ -84,6 +86,38 @@ ra_status launch_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const
 // fp32 -> bf16 copy of n elements (n a multiple of 4): the stepwise ring finish
 ra_status launch_f32_to_bf16(const float *src, void *dst, int64_t n, cudaStream_t stream,
                              const char **err);
+
+// The 4-D view of a [..., cols] tensor that the attention kernels' TMA maps
+// use (tile_coords gives a tile's coordinates in it): the columns, then three
+// outer extents n[] with their element strides st[]; rows are outer dimension
+// row_dim (0 or 1).  Shard stacks [stacks, B, S, cols]; in token order
+// ([B, L, cols], L = N*S) the layout's view: contiguous [B, N, S], striped
+// [B, S, N] (position s*N + r), zigzag [B, 2N, S/2].
+struct TileView {
+    int64_t n[3], st[3];
+    int row_dim;
+};
+inline TileView tile_view(bool seq_order, int layout, int64_t S, int64_t B, int64_t N, int64_t stacks,
+                          int64_t cols) {
+    TileView v;
+    v.row_dim = 0;
+    if (!seq_order) {
+        v.n[0] = S, v.n[1] = B, v.n[2] = stacks;
+        v.st[0] = cols, v.st[1] = S * cols, v.st[2] = B * S * cols;
+    } else if (layout == RA_STRIPED) {
+        v.n[0] = N, v.n[1] = S, v.n[2] = B;
+        v.st[0] = cols, v.st[1] = N * cols, v.st[2] = N * S * cols;
+        v.row_dim = 1;
+    } else if (layout == RA_ZIGZAG) {
+        const int64_t C = S / 2;
+        v.n[0] = C, v.n[1] = 2 * N, v.n[2] = B;
+        v.st[0] = cols, v.st[1] = C * cols, v.st[2] = N * S * cols;
+    } else {
+        v.n[0] = S, v.n[1] = N, v.n[2] = B;
+        v.st[0] = cols, v.st[1] = S * cols, v.st[2] = N * S * cols;
+    }
+    return v;
+}
 
 // Record `msg` as this host thread's ra_last_error() text and return `st`.
 ra_status set_error(ra_status st, const char *msg);

@@ -79,4 +79,36 @@ struct TileWalk {
     }
 };
 
+// The outer TMA coordinates (after the column) of local rows [row, row + 128)
+// of rank `rank`'s shard of batch b, for the views tile_view describes.
+// Shard stacks [N or 1, B, S, cols] are addressed (row, b, rank).  In token
+// order the layout is the addressing: contiguous {S, N, B} (position r*S + s),
+// striped {N, S, B} (position s*N + r, the row is the second coordinate),
+// zigzag {C, 2N, B} with C = S/2 (rank r's rows are chunk r, then chunk
+// 2N-1-r; C is a multiple of 128, so a 128-row tile never straddles the two).
+// Rows past a shard's end fall outside the view: loads read zeros there and
+// stores skip them.
+__device__ __forceinline__ void tile_coords(int seq_order, int layout, int S, int N, int rank, int b, int row,
+                                            int &c1, int &c2, int &c3) {
+    if (!seq_order) {
+        c1 = row;
+        c2 = b;
+        c3 = rank;
+    } else if (layout == RA_STRIPED) {
+        c1 = rank;
+        c2 = row;
+        c3 = b;
+    } else if (layout == RA_ZIGZAG) {
+        const int C = S >> 1;
+        const bool hi = row >= C;
+        c1 = hi ? row - C : row;
+        c2 = hi ? 2 * N - 1 - rank : rank;
+        c3 = b;
+    } else {
+        c1 = row;
+        c2 = rank;
+        c3 = b;
+    }
+}
+
 }  // namespace ra

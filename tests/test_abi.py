@@ -154,3 +154,22 @@ def test_launch_chunk_pairs(ralib, monkeypatch):
     for bad in ("0", "-5", "abc", ""):
         monkeypatch.setenv("RA_L2_CHUNK_KB", bad)
         assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3, bad
+
+
+def _bwd(ralib, **kw):
+    a = dict(B=1, L=1024, H=2, Hkv=2, d=128, N=4, layout=0, causal=1, scale=0.0, flags=0)
+    a.update(kw)
+    return ralib.lib().ra_ring_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0,
+                                        a["B"], a["L"], a["H"], a["Hkv"], a["d"], a["N"], a["layout"],
+                                        a["causal"], a["scale"], a["flags"], FAKE, 16, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=1), 1),                        # only RA_FLAG_SEQ_ORDER applies to the backward
+    (dict(flags=4, layout=2, L=1280), 3),      # token-order zigzag: chunk 160 is not a multiple of 128
+    (dict(flags=4), 1),                        # then the small workspace is rejected
+    (dict(d=96), 3),
+])
+def test_backward_rejects_bad_arguments(ralib, kw, status):
+    assert _bwd(ralib, **kw) == status
+    assert ralib.lib().ra_last_error().decode()
