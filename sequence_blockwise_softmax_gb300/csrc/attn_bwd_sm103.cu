@@ -38,6 +38,11 @@
 // threads, two per tensor-memory lane: warps 4-7 take the first 64 columns of
 // a tile and warps 8-11 the last 64 (no product here reduces along a row, so
 // the halves never exchange data).  Every wait is bounded.
+//
+// Operands come through the forward's 4-D views (shard stacks or token order,
+// tile_view / tile_coords); in token order the gradient rows are stored at
+// their token positions, and the dot kernel leaves D and a copy of LSE in
+// stack order so that both passes read a tile's vectors contiguously.
 #include <cmath>
 
 #include "ra_device.cuh"

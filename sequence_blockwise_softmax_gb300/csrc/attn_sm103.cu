@@ -40,6 +40,12 @@
 // releases S_g once P is computed and its denominator checked (the rare
 // second pass reloads S), and each tile's critical chain is S -> softmax ->
 // PV with no wait on the previous PV in between.
+//
+// Addressing: every tile moves through a 4-D tensor map of either the shard
+// stacks [N, B, S, H, d] or the token-order tensors [B, L, H, d]
+// (tile_view / tile_coords).  In token order a layout is only a choice of view
+// (§4, §6.1 of the same article), so the sweep reads each rank's shard and
+// writes its result in place and no permute runs.
 #include <cmath>
 #include <cstdio>
 
