@@ -173,3 +173,31 @@ def _bwd(ralib, **kw):
 def test_backward_rejects_bad_arguments(ralib, kw, status):
     assert _bwd(ralib, **kw) == status
     assert ralib.lib().ra_last_error().decode()
+
+
+def _ctype_of(decl):
+    """ctypes class of one C parameter or return declaration of include/ra.h."""
+    decl = " ".join(decl.replace("const", " ").split())
+    if decl.startswith("char *") or decl == "char *":
+        return ctypes.c_char_p
+    if "*" in decl:
+        return ctypes.c_void_p
+    base = decl.split()[0]
+    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "unsigned": ctypes.c_uint,
+            "float": ctypes.c_float, "size_t": ctypes.c_size_t, "ra_status": ctypes.c_int}[base]
+
+
+def test_binding_signatures_match_the_header(ralib):
+    """Every prototype's return and parameter types, as the Python binding declares them to
+    ctypes: a parameter added to a C call without its ctypes slot would shift every argument
+    after it."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = re.findall(r"^RA_API\s+([\w\s\*]*?)\b(ra_\w+)\s*\(([^)]*)\)\s*;", src, flags=re.M)
+    assert len(protos) == len(ralib.SIGNATURES)
+    for ret, name, params in protos:
+        params = params.strip()
+        args = [] if params in ("", "void") else [_ctype_of(p.rsplit(None, 1)[0] if "*" not in p.split()[-1]
+                                                           else p[:p.rfind("*") + 1]) for p in params.split(",")]
+        want_ret, want_args = ralib.SIGNATURES[name]
+        assert _ctype_of(ret.strip()) is want_ret, name
+        assert args == list(want_args), name
