@@ -88,8 +88,8 @@ struct TileWalk {
 // 2N-1-r; C is a multiple of 128, so a 128-row tile never straddles the two).
 // Rows past a shard's end fall outside the view: loads read zeros there and
 // stores skip them.
-__device__ __forceinline__ void tile_coords(int seq_order, int layout, int S, int N, int rank, int b, int row,
-                                            int &c1, int &c2, int &c3) {
+__host__ __device__ __forceinline__ void tile_coords(int seq_order, int layout, int S, int N, int rank, int b,
+                                                     int row, int &c1, int &c2, int &c3) {
     if (!seq_order) {
         c1 = row;
         c2 = b;
