@@ -17,7 +17,8 @@
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates device memory and keeps no pointer after a call returns.
- *   - Every pointer must be 16-byte aligned (RA_ERR_ALIGNMENT otherwise).
+ *   - Every pointer must be 16-byte aligned (RA_ERR_ALIGNMENT otherwise),
+ *     unless its call states a weaker rule.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous and stream-ordered.
  *   - Arguments are checked on the host before anything is launched; a failed
@@ -77,11 +78,11 @@ typedef enum {
 /* Launch order.  Causal work grows with position, so the attention kernels
  * (forward and both backward passes) run heavy units first.  They take
  * (batch, head) pairs in chunks whose streamed keys and values (queries and dO
- * in the dK/dV pass) fit in L2 together, about 48 MB per chunk (all pairs
- * at once when they fit in about 80 MB), and interleave the units of a
- * chunk's pairs heaviest first.  The environment
- * variable RA_L2_CHUNK_KB, read at every launch, sets that budget in KiB (a
- * positive integer; anything else keeps the default).  The order never
+ * in the dK/dV pass) fit in L2 together, 48 MiB per chunk by default (all
+ * pairs at once when they fit in 5/3 of that), and interleave the units of a
+ * chunk's pairs heaviest first.  ra_set_launch_chunk_budget() changes the
+ * budget for the whole process (the one setting this library keeps besides
+ * the error text); nothing is read from the environment.  The order never
  * changes a result: every unit's arithmetic is independent of when it runs. */
 
 /* ra_ring_attn_fwd flags */
@@ -98,8 +99,8 @@ typedef enum {
  * zigzag needs its chunk L / 2N to be a multiple of 128 (RA_ERR_UNSUPPORTED
  * otherwise).  There is no Ulysses split in this form (U = 1).            */
 #define RA_FLAG_SEQ_ORDER 4u
-/* Test hook for the timeout path: the first CTA of the fused sweep never
- * loads one key tile, so the waits that depend on it run out after about two
+/* Test hook for the timeout path: the first CTA of the fused sweep (or of
+ * the first step of ra_ring_attn_fwd_stepwise_noalloc) never loads one key tile, so the waits that depend on it run out after about two
  * seconds; the kernel records RA_ERR_TIMEOUT in the status word, releases what
  * it holds and exits, and the outputs of that CTA are left unwritten.  Nothing
  * faults and the context stays usable.  Not for production use.              */
@@ -164,12 +165,27 @@ RA_API ra_status ra_block_attn_fwd(const void *q, const void *k, const void *v, 
  * ra_lse_merge -- fold partial result b into accumulator acc, in place
  * ([USP] §6.3):  lse = max(lse_a, lse_b) + ln(1 + exp(-|lse_a - lse_b|)),
  *                O   = O_a exp(lse_a - lse) + O_b exp(lse_b - lse).
- * o_acc, o_b: fp32 [B, S, H, d]; lse_acc, lse_b: fp32 [B, H, S].
- * -inf marks an empty partial: it gets weight 0, and two empty partials stay
- * (O = 0, lse = -inf).  d is a multiple of 4, at most 256.
+ * `rows` rows of d fp32 values: row r of the accumulator's O starts at
+ * o_acc + r * acc_row_stride and row r of b's at o_b + r * b_row_stride
+ * (strides in floats, multiples of 4 and at least d, so O may be a strided
+ * view, e.g. one head of a [.., S, H, d] tensor with stride H * d); their
+ * LSEs are lse_acc[r] and lse_b[r] (fp32, contiguous).  O pointers 16-byte
+ * aligned, LSE pointers 4-byte aligned.  -inf marks an empty partial: it gets
+ * weight 0, and two empty partials stay (O = 0, lse = -inf).  d is a multiple
+ * of 4, at most 256.  Rows must not overlap between acc and b.
  */
 RA_API ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
-                       int64_t B, int64_t S, int64_t H, int d, void *stream);
+                              int64_t rows, int d, int64_t acc_row_stride, int64_t b_row_stride,
+                              void *stream);
+
+/*
+ * ra_lse_merge_bshd -- the same merge over whole ring-call tensors:
+ * o_acc, o_b fp32 [B, S, H, d]; lse_acc, lse_b fp32 [B, H, S] (the layouts
+ * ra_block_attn_fwd writes).  Equivalent to B * H strided ra_lse_merge calls
+ * (rows = S, strides H * d), in one launch.  Every pointer 16-byte aligned.
+ */
+RA_API ra_status ra_lse_merge_bshd(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
+                                   int64_t B, int64_t S, int64_t H, int d, void *stream);
 
 /*
  * ra_ring_attn_fwd -- the whole ring sweep ([USP] §3.1-§3.3): for every rank
@@ -242,21 +258,36 @@ RA_API size_t ra_ring_attn_workspace_bytes(int64_t B, int64_t L, int64_t H, int 
  * outputs, paths where cudaMalloc / cudaFree would synchronise the device.
  * Its scratch (one fp32 partial O and LSE plus a status word) is a fixed
  * 64 MiB array owned by the library, held on every GPU that loads this code
- * until the process exits; a problem needing more than
- * B*L*H*(d+1)*4 + 256 <= 64 MiB bytes is rejected with RA_ERR_UNSUPPORTED.
- * Arguments and layouts are those of ra_ring_attn_fwd with flags =
- * RA_FLAG_STEPWISE; o is fp32.  It allocates nothing.  The first call on
- * each device looks up the array's device address (which loads this part of
- * the library on that device); make that first call before any stream
+ * until the process exits.  A problem is accepted when
+ *     256 + round256(B*L*H*d*4) + round256(B*L*H*4) <= 64 MiB
+ * (round256: up to a multiple of 256 bytes), else RA_ERR_UNSUPPORTED.
+ * Arguments, checks and layouts are those of ra_ring_attn_fwd with flags =
+ * RA_FLAG_STEPWISE; o is fp32.  flags: 0, or the test hook
+ * RA_FLAG_INJECT_STALL (the first step's launch withholds one key tile, so its
+ * waits run out as described there).  It allocates nothing.  The first call
+ * on each device looks up the array's device address (which loads this part
+ * of the library on that device); make that first call before any stream
  * capture.  Every call on a device uses the same array: calls that may
  * overlap on the GPU (other streams, other threads) race on it and must be
- * serialised by the caller.  The status word is cleared at the start of each
- * call; a wait that runs out is not reported back by this entry point.
+ * serialised by the caller.  A wait that runs out is recorded in the array's
+ * status word, which keeps it across calls until ra_noalloc_check_status()
+ * reports and clears it.
  */
 RA_API ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void *k, const void *v,
                                                    float *o, float *lse, int64_t B, int64_t L,
                                                    int64_t H, int d, int N, int layout,
-                                                   int causal, float scale, void *stream);
+                                                   int causal, float scale, unsigned flags,
+                                                   void *stream);
+
+/*
+ * ra_noalloc_check_status -- synchronise `stream`, read the status word of
+ * the current device's scratch array, clear it, and return RA_ERR_TIMEOUT if
+ * a kernel of ra_ring_attn_fwd_stepwise_noalloc gave up on a bounded wait
+ * since the last check (its outputs are then incomplete), RA_ERR_ALIGNMENT
+ * if one found its shared memory base unaligned, RA_OK otherwise.  It
+ * allocates nothing.
+ */
+RA_API ra_status ra_noalloc_check_status(void *stream);
 
 /*
  * ra_ring_attn_bwd -- gradients of ra_ring_attn_fwd.  The pages describe the
@@ -304,14 +335,29 @@ RA_API const char *ra_last_error(void);
 /* Library version string. */
 RA_API const char *ra_version(void);
 
+/* ra_ring_step_pairs -- how many (query, key) pairs query shard q_rank and
+ * key/value shard kv_rank have in common under `layout` over N ranks of S
+ * tokens: S * S without the causal mask, else the pairs whose key position is
+ * not after the query's ([USP] §3.4; the count the attention kernels' masks
+ * give).  0 means a ring step with nothing to compute (contiguous, a later
+ * rank's shard).  Host only, O(S); -1 on bad arguments. */
+RA_API int64_t ra_ring_step_pairs(int layout, int64_t S, int N, int q_rank, int kv_rank, int causal);
+
+/* ra_set_launch_chunk_budget -- set the launch-order chunk budget (see
+ * "Launch order" above) to `bytes` for every later launch in the process;
+ * bytes <= 0 restores the default of 48 MiB.  Returns the previous budget.
+ * Host only; it never changes a result, only the order units run in. */
+RA_API int64_t ra_set_launch_chunk_budget(int64_t bytes);
+
 /* ra_launch_chunk_pairs -- how many (batch, head) pairs the attention kernels
  * interleave per chunk of their launch order (see "Launch order" above) when a
- * pair streams per_pair_bytes.  With B the budget (RA_L2_CHUNK_KB, else 48
- * MiB): all pairs if they stream at most 5/3 B together (one chunk: the
- * whole launch runs heaviest units first); otherwise the fewest chunks of at
- * most B each, made near-equal (ceil(pairs / n) pairs for n = ceil(pairs /
- * floor(B / per_pair_bytes))), at least 1.  Host only; launches nothing.
- * Returns 1 for per_pair_bytes <= 0 and pairs for pairs < 1. */
+ * pair streams per_pair_bytes.  With B the budget (48 MiB unless
+ * ra_set_launch_chunk_budget changed it): all pairs if they stream at most
+ * 5/3 B together (one chunk: the whole launch runs heaviest units first);
+ * otherwise the fewest chunks of at most B each, made near-equal
+ * (ceil(pairs / n) pairs for n = ceil(pairs / floor(B / per_pair_bytes))), at
+ * least 1.  Host only; launches nothing.  Returns 1 for per_pair_bytes <= 0
+ * and pairs for pairs < 1. */
 RA_API int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs);
 
 #ifdef __cplusplus

@@ -35,7 +35,8 @@ SIGNATURES = {
     "ra_lse_to_seq": (_I, [_P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
     "ra_block_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _I, _I, _F,
                                _P, _SZ, _P]),
-    "ra_lse_merge": (_I, [_P, _P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "ra_lse_merge": (_I, [_P, _P, _P, _P, _I64, _I, _I64, _I64, _P]),
+    "ra_lse_merge_bshd": (_I, [_P, _P, _P, _P, _I64, _I64, _I64, _I, _P]),
     "ra_ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I, _F, _U, _P,
                               _SZ, _P]),
     "ra_ring_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I, _U]),
@@ -46,13 +47,16 @@ SIGNATURES = {
     "ra_ring_attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _I, _I, _F,
                                      _U, _P, _SZ, _P]),
     "ra_ring_attn_fwd_stepwise_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _I,
-                                               _F, _P]),
+                                               _F, _U, _P]),
+    "ra_noalloc_check_status": (_I, [_P]),
     "ra_ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I64, _I, _I,
                               _I, _I, _F, _U, _P, _SZ, _P]),
     "ra_ring_attn_bwd_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "ra_check_status": (_I, [_P, _P]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),
+    "ra_ring_step_pairs": (_I64, [_I, _I64, _I, _I, _I, _I]),
+    "ra_set_launch_chunk_budget": (_I64, [_I64]),
     "ra_launch_chunk_pairs": (_I64, [_I64, _I64]),
 }
 
@@ -136,9 +140,32 @@ def ra_block_attn_fwd(q, k, v, o, lse, B, S, H, d, N, q_rank, kv_rank, layout, c
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def ra_lse_merge(o_acc, lse_acc, o_b, lse_b, B, S, H, d, stream=None):
-    _check(lib().ra_lse_merge(_ptr(o_acc, "o_acc"), _ptr(lse_acc, "lse_acc"), _ptr(o_b, "o_b"),
-                              _ptr(lse_b, "lse_b"), B, S, H, d, _stream(stream)))
+def _ptr_view(t, name):
+    """Device pointer of a CUDA tensor that may be a strided view (the C call takes strides)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t.data_ptr()
+
+
+def ra_lse_merge(o_acc, lse_acc, o_b, lse_b, stream=None):
+    """Strided merge: o_acc, o_b are [rows, d] fp32 views whose rows may be strided (unit
+    stride along d); lse_acc, lse_b are contiguous [rows] fp32."""
+    for t in (o_acc, o_b):
+        assert t.dtype == torch.float32 and t.dim() == 2 and t.stride(1) == 1
+    for t in (lse_acc, lse_b):
+        assert t.dtype == torch.float32 and t.dim() == 1 and t.is_contiguous()
+    rows, d = o_acc.shape
+    assert o_b.shape == (rows, d) and lse_acc.numel() == rows and lse_b.numel() == rows
+    _check(lib().ra_lse_merge(_ptr_view(o_acc, "o_acc"), _ptr(lse_acc, "lse_acc"), _ptr_view(o_b, "o_b"),
+                              _ptr(lse_b, "lse_b"), rows, d, o_acc.stride(0), o_b.stride(0),
+                              _stream(stream)))
+
+
+def ra_lse_merge_bshd(o_acc, lse_acc, o_b, lse_b, B, S, H, d, stream=None):
+    _check(lib().ra_lse_merge_bshd(_ptr(o_acc, "o_acc"), _ptr(lse_acc, "lse_acc"), _ptr(o_b, "o_b"),
+                                   _ptr(lse_b, "lse_b"), B, S, H, d, _stream(stream)))
 
 
 def ra_ring_attn_workspace_bytes(B, L, H, d, N, flags=0):
@@ -161,7 +188,7 @@ def ra_ring_attn_fwd(q, k, v, o, lse, B, L, H, d, N, layout, causal, scale=0.0, 
 
 
 def ra_ring_attn_fwd_stepwise_noalloc(q, k, v, o, lse, B, L, H, d, N, layout, causal, scale=0.0,
-                                      stream=None):
+                                      flags=0, stream=None):
     """Stepwise sweep with the library's own fixed scratch array; O is fp32."""
     for t in (q, k, v):
         assert t.dtype == torch.bfloat16
@@ -169,7 +196,11 @@ def ra_ring_attn_fwd_stepwise_noalloc(q, k, v, o, lse, B, L, H, d, N, layout, ca
     _check(lib().ra_ring_attn_fwd_stepwise_noalloc(_ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"),
                                                    _ptr(o, "o"), _ptr(lse, "lse"), B, L, H, d, N,
                                                    _layout(layout), int(bool(causal)), float(scale),
-                                                   _stream(stream)))
+                                                   int(flags), _stream(stream)))
+
+
+def ra_noalloc_check_status(stream=None):
+    _check(lib().ra_noalloc_check_status(_stream(stream)))
 
 
 def ra_block_attn_fwd_gqa(q, k, v, o, lse, B, S, H, H_kv, d, N, q_rank, kv_rank, layout, causal,
@@ -247,6 +278,20 @@ def ra_check_status(workspace, stream=None):
 
 def ra_version():
     return lib().ra_version().decode()
+
+
+def ra_ring_step_pairs(layout, S, N, q_rank, kv_rank, causal):
+    """Visible (query, key) pairs of query shard q_rank against key/value shard kv_rank."""
+    n = int(lib().ra_ring_step_pairs(_layout(layout), int(S), int(N), int(q_rank), int(kv_rank),
+                                     int(bool(causal))))
+    if n < 0:
+        raise RAError(RA_ERR_INVALID_ARG, "bad arguments to ra_ring_step_pairs")
+    return n
+
+
+def ra_set_launch_chunk_budget(nbytes):
+    """Set the launch-order chunk budget (<= 0: the default); returns the previous one."""
+    return int(lib().ra_set_launch_chunk_budget(int(nbytes)))
 
 
 def ra_launch_chunk_pairs(per_pair_bytes, pairs):

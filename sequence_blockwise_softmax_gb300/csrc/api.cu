@@ -1,13 +1,14 @@
 // api.cu -- the C ABI (include/ra.h): argument checks, workspace layout and
 // launch order.  Every check runs on the host before any CUDA call, so a
 // rejected call touches neither the device nor the stream.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
-#include <cstdlib>
 #include <string>
 
 #include "ra_internal.h"
+#include "ra_positions.cuh"
 
 namespace {
 
@@ -68,21 +69,40 @@ ra_status check_attn_common(int64_t B, int64_t S, int64_t H, int d, int N, int l
 
 ra_status ra::set_error(ra_status st, const char *msg) { return fail(st, msg); }
 
-int64_t ra::l2_chunk_bytes() {
-    const char *e = std::getenv("RA_L2_CHUNK_KB");
-    if (e != nullptr) {
-        char *end = nullptr;
-        const long long kb = std::strtoll(e, &end, 10);
-        if (end != e && kb > 0) return (int64_t)kb << 10;
-    }
-    return (int64_t)48 << 20;
+ra_status ra::check_attn_sizes(int64_t B, int64_t S, int64_t H, int d, int N, int layout, float scale) {
+    return check_attn_common(B, S, H, d, N, layout, scale);
 }
+
+namespace {
+constexpr int64_t kDefaultChunkBytes = (int64_t)48 << 20;
+std::atomic<int64_t> g_chunk_bytes{kDefaultChunkBytes};
+}  // namespace
+
+int64_t ra::l2_chunk_bytes() { return g_chunk_bytes.load(std::memory_order_relaxed); }
 
 extern "C" {
 
 const char *ra_last_error(void) { return g_last_error.c_str(); }
 
 const char *ra_version(void) { return "ra_gb300 0.1 (sm_103a)"; }
+
+int64_t ra_set_launch_chunk_budget(int64_t bytes) {
+    const int64_t prev = g_chunk_bytes.load();
+    g_chunk_bytes.store(bytes > 0 ? bytes : kDefaultChunkBytes);
+    return prev;
+}
+
+int64_t ra_ring_step_pairs(int layout, int64_t S, int N, int q_rank, int kv_rank, int causal) {
+    if (!valid_layout(layout) || N < 1 || S < 0 || q_rank < 0 || q_rank >= N || kv_rank < 0 || kv_rank >= N)
+        return -1;
+    if (layout == RA_ZIGZAG && (S % 2)) return -1;
+    if (S > ((int64_t)1 << 30)) return -1;
+    if (!causal) return S * S;
+    int64_t pairs = 0;
+    for (int64_t a = 0; a < S; ++a)
+        pairs += ra::keys_upto(layout, kv_rank, ra::token_pos(layout, q_rank, a, N, S), N, S);
+    return pairs;
+}
 
 int64_t ra_launch_chunk_pairs(int64_t per_pair_bytes, int64_t pairs) {
     if (pairs < 1) return pairs;
@@ -216,11 +236,36 @@ ra_status ra_block_attn_fwd_gqa(const void *q, const void *k, const void *v, flo
                       workspace, workspace_bytes, stream);
 }
 
-ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b, int64_t B,
-                       int64_t S, int64_t H, int d, void *stream) {
+ra_status ra_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b, int64_t rows,
+                       int d, int64_t acc_row_stride, int64_t b_row_stride, void *stream) {
+    if (rows < 0 || d < 0) return fail(RA_ERR_SHAPE, "rows and d must be non-negative");
+    if (d % 4 || d > 256) return fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4, at most 256");
+    if (rows == 0 || d == 0) return RA_OK;
+    if (acc_row_stride < d || b_row_stride < d)
+        return fail(RA_ERR_SHAPE, "a row stride is smaller than d: rows would overlap");
+    if (acc_row_stride % 4 || b_row_stride % 4)
+        return fail(RA_ERR_ALIGNMENT, "row strides must be multiples of 4 floats (16 bytes)");
+    if (rows > ((int64_t)1 << 40) / acc_row_stride || rows > ((int64_t)1 << 40) / b_row_stride)
+        return fail(RA_ERR_UNSUPPORTED, "rows * row stride beyond the supported range");
+    if (!o_acc || !lse_acc || !o_b || !lse_b) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(o_acc) || !aligned16(o_b))
+        return fail(RA_ERR_ALIGNMENT, "the O pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(lse_acc) & 3u) || (reinterpret_cast<uintptr_t>(lse_b) & 3u))
+        return fail(RA_ERR_ALIGNMENT, "the LSE pointers must be 4-byte aligned");
+    const char *err = nullptr;
+    ra_status st = ra::launch_lse_merge_rows(o_acc, lse_acc, o_b, lse_b, rows, d, acc_row_stride, b_row_stride,
+                                             static_cast<cudaStream_t>(stream), &err);
+    return st == RA_OK ? st : fail(st, err ? err : "merge launch failed");
+}
+
+ra_status ra_lse_merge_bshd(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b, int64_t B,
+                            int64_t S, int64_t H, int d, void *stream) {
     if (B < 0 || S < 0 || H < 0 || d < 0) return fail(RA_ERR_SHAPE, "sizes must be non-negative");
     if (d % 4 || d > 256) return fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4, at most 256");
     if (B * S * H * d == 0) return RA_OK;
+    if (B > ((int64_t)1 << 20) || H > ((int64_t)1 << 20) || S > ((int64_t)1 << 30) ||
+        B * S * H * d > ((int64_t)1 << 40))
+        return fail(RA_ERR_UNSUPPORTED, "B, S, H beyond the supported range");
     if (!o_acc || !lse_acc || !o_b || !lse_b) return fail(RA_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned16(o_acc) || !aligned16(lse_acc) || !aligned16(o_b) || !aligned16(lse_b))
         return fail(RA_ERR_ALIGNMENT, "every pointer must be 16-byte aligned");

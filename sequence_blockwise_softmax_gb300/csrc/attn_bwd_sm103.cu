@@ -71,20 +71,6 @@ struct BwdArgs {
     int seq_order;          // token-order tensors (the layout is the tiles' addresses)
 };
 
-// Tile decode shared by both passes: (batch, head) pairs are taken in chunks
-// of `chunk` whose streamed operands fit in L2 together, and inside a chunk
-// the tiles of all its pairs are interleaved, so that the heaviest tiles of
-// every pair come first.  Returns the pair and the tile's rank within it.
-__device__ __forceinline__ void bwd_decode(int block, int per_bh, int BH, int chunk, int &bh, int &rem) {
-    const int per_chunk = chunk * per_bh;
-    const int c = block / per_chunk;
-    const int c_first = c * chunk;
-    const int c_size = min(chunk, BH - c_first);
-    const int idx = block - c * per_chunk;
-    bh = c_first + idx % c_size;
-    rem = idx / c_size;
-}
-
 __device__ __forceinline__ uint8_t *bwd_align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -255,43 +241,17 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int S = args.S, H = args.H, N = args.N;
-    const int per_bh = N * args.n_tiles_seq;
-    int bh, rem;
-    bwd_decode(blockIdx.x, per_bh, args.B * H, args.bh_chunk_q, bh, rem);
-    const int b = bh / H, h = bh % H;
     // causal work grows with the query position: heaviest tiles first
-    int qi, qt;
-    if (args.layout == RA_CONTIGUOUS) {
-        qi = N - 1 - rem / args.n_tiles_seq;
-        qt = args.n_tiles_seq - 1 - rem % args.n_tiles_seq;
-    } else {
-        qt = args.n_tiles_seq - 1 - rem / N;
-        qi = N - 1 - rem % N;
-    }
+    const UnitId unit = decode_unit(blockIdx.x, args.bh_chunk_q, args.B, H, N, args.n_tiles_seq, args.layout);
+    const int b = unit.b, h = unit.h, qi = unit.qi, qt = unit.qt;
     const int zq = qi * args.B + b;
     const int row0 = qt * 128;
     const int row_end = min(S, row0 + 128);
     const int hk = h / (H / args.Hkv);
     const int64_t total = (int64_t)N * S;
 
-    TileWalk walk0;
-    walk0.step = 0;
-    walk0.num_steps = N;
-    walk0.step_base = 0;
-    walk0.q_rank = qi;
-    walk0.kv_fixed = -1;
-    walk0.N = N;
-    walk0.layout = args.layout;
-    walk0.S = S;
-    {
-        const int64_t first_pos = token_pos(args.layout, qi, row0, N, S);
-        const int64_t last_pos = token_pos(args.layout, qi, row_end - 1, N, S);
-        int64_t fs, fe, ls, le;
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, fs, fe);
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, ls, le);
-        walk0.lo_pos = fs - 1;
-        walk0.hi_pos = args.causal ? last_pos : le - 1;
-    }
+    const TileWalk walk0 = unit_walk(args.layout, N, S, qi, -1, N, 0, row0, row_end, args.causal, args.cu_seqlens,
+                                     args.n_seqs);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QFULL), 1);
@@ -457,9 +417,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128, tQ = tmem + lane_off + 256;
         const int64_t my_pos = token_pos(args.layout, qi, a_c, N, S);
-        int64_t my_start, my_end;
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, my_pos, my_start, my_end);
-        const int64_t lo_pos = my_start - 1, hi_pos = args.causal ? my_pos : my_end - 1;
+        int64_t lo_pos, hi_pos;
+        row_key_bounds(args.cu_seqlens, args.n_seqs, total, my_pos, args.causal, lo_pos, hi_pos);
         const size_t vi = ((size_t)zq * H + h) * S + a_c;
         const float lse_v = args.lse[vi];
         const float lse2 = lse_v > -INFINITY ? lse_v * 1.4426950408889634f : 0.f;   // no key: P = 0 anyway
@@ -585,39 +544,6 @@ struct BwdKVSmem {
     static constexpr uint32_t kBytes = kMisc + 16;
 };
 
-// The query tiles a block of keys meets, for each query head of its group and
-// each query rank in ring order (j, j+1, ...): for keys at positions
-// first_pos..last_pos the visible queries of rank i are the local interval
-// [keys_upto(i, lo_pos), keys_upto(i, hi_pos)).
-struct QWalk {
-    int head, step, tile, tile_end, i;
-    int heads, N, j, layout, S;
-    int64_t lo_pos, hi_pos;
-
-    __device__ void start() {
-        while (head < heads) {
-            while (step < N) {
-                i = (j + step) % N;
-                const int64_t lo = keys_upto(layout, i, lo_pos, N, S);
-                const int64_t hi = keys_upto(layout, i, hi_pos, N, S);
-                tile = (int)(lo / 128);
-                tile_end = (int)((hi + 127) / 128);
-                if (tile_end > tile) return;
-                ++step;
-            }
-            step = 0;
-            ++head;
-        }
-    }
-    __device__ bool valid() const { return head < heads; }
-    __device__ void next() {
-        if (++tile >= tile_end) {
-            ++step;
-            start();
-        }
-    }
-};
-
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -645,41 +571,17 @@ __global__ void __launch_bounds__(384, 1)
 
     const int S = args.S, H = args.H, N = args.N, Hkv = args.Hkv;
     const int group = H / Hkv;
-    const int per_bh = N * args.n_tiles_seq;
-    int bh, rem;
-    bwd_decode(blockIdx.x, per_bh, args.B * Hkv, args.bh_chunk_kv, bh, rem);
-    const int b = bh / Hkv, hk = bh % Hkv;
     // causal work shrinks with the key position: earliest keys first
-    int kj, kt;
-    if (args.layout == RA_CONTIGUOUS) {
-        kj = rem / args.n_tiles_seq;
-        kt = rem % args.n_tiles_seq;
-    } else {
-        kt = rem / N;
-        kj = rem % N;
-    }
+    const UnitId unit = decode_key_block(blockIdx.x, args.bh_chunk_kv, args.B, Hkv, N, args.n_tiles_seq,
+                                         args.layout);
+    const int b = unit.b, hk = unit.h, kj = unit.qi, kt = unit.qt;
     const int zk = kj * args.B + b;
     const int c0 = kt * 128;
     const int c_end = min(S, c0 + 128);
     const int64_t total = (int64_t)N * S;
 
-    QWalk walk0;
-    walk0.head = 0;
-    walk0.step = 0;
-    walk0.heads = group;
-    walk0.N = N;
-    walk0.j = kj;
-    walk0.layout = args.layout;
-    walk0.S = S;
-    {
-        const int64_t first_pos = token_pos(args.layout, kj, c0, N, S);
-        const int64_t last_pos = token_pos(args.layout, kj, c_end - 1, N, S);
-        int64_t fs, fe, ls, le;
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, fs, fe);
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, ls, le);
-        walk0.lo_pos = args.causal ? first_pos - 1 : fs - 1;
-        walk0.hi_pos = le - 1;
-    }
+    const QWalk walk0 = key_block_walk(args.layout, N, S, kj, group, c0, c_end, args.causal, args.cu_seqlens,
+                                       args.n_seqs);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_KVFULL), 1);
@@ -867,9 +769,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128;
         const uint32_t tV = tmem + lane_off + 256, tK = tmem + lane_off + 256 + D;
         const int64_t kpos = token_pos(args.layout, kj, kk_c, N, S);
-        int64_t ks, ke;
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, kpos, ks, ke);
-        const int64_t lo_pos = args.causal ? kpos - 1 : ks - 1, hi_pos = ke - 1;
+        int64_t lo_pos, hi_pos;
+        col_query_bounds(args.cu_seqlens, args.n_seqs, total, kpos, args.causal, lo_pos, hi_pos);
         const float sl2 = args.scale_log2;
         QWalk w = walk0;
         w.start();

@@ -195,55 +195,20 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- unit decode: heavy units first (causal work grows with position).
-    // The (batch, head) pairs are taken in chunks of bh_chunk whose keys and
-    // values fit in L2 together; inside a chunk the units of all its pairs are
-    // interleaved, heaviest first, so no pair's heavy units are left for the
-    // tail of the launch.
+    // ---- unit decode: heavy units first, in L2-sized chunks of (batch, head)
+    // pairs (decode_unit)
     const int S = args.S, H = args.H, N = args.N;
-    const int per_bh = args.num_q_ranks * args.n_units_seq;
-    const int BH = args.B * H;
-    const int per_chunk = args.bh_chunk * per_bh;
-    const int chunk = blockIdx.x / per_chunk;
-    const int c_first = chunk * args.bh_chunk;
-    const int c_size = min(args.bh_chunk, BH - c_first);
-    const int idx = blockIdx.x - chunk * per_chunk;
-    const int bh = c_first + idx % c_size;
-    const int rem = idx / c_size;
-    const int b = bh / H, h = bh % H;
-    int qi, qt;
-    if (args.layout == RA_CONTIGUOUS) {
-        qi = args.num_q_ranks - 1 - rem / args.n_units_seq;
-        qt = args.n_units_seq - 1 - rem % args.n_units_seq;
-    } else {
-        qt = args.n_units_seq - 1 - rem / args.num_q_ranks;
-        qi = args.num_q_ranks - 1 - rem % args.num_q_ranks;
-    }
+    const UnitId unit = decode_unit(blockIdx.x, args.bh_chunk, args.B, H, args.num_q_ranks, args.n_units_seq,
+                                    args.layout);
+    const int b = unit.b, h = unit.h, qi = unit.qi, qt = unit.qt;
     const bool ring = args.q_rank_fixed < 0;
     const int q_rank = ring ? qi : args.q_rank_fixed;
     const int zq = (ring ? qi * args.B : 0) + b;
     const int row0 = qt * 256;
     const int row_end = min(S, row0 + 256);
 
-    TileWalk walk0;
-    walk0.step = 0;
-    walk0.num_steps = args.num_steps;
-    walk0.step_base = args.step_base;
-    walk0.q_rank = q_rank;
-    walk0.kv_fixed = args.kv_rank_fixed;
-    walk0.N = N;
-    walk0.layout = args.layout;
-    walk0.S = S;
-    {
-        const int64_t total = (int64_t)N * S;
-        const int64_t first_pos = token_pos(args.layout, q_rank, row0, N, S);
-        const int64_t last_pos = token_pos(args.layout, q_rank, row_end - 1, N, S);
-        int64_t first_start, first_end, last_start, last_end;
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, first_pos, first_start, first_end);
-        seq_bounds(args.cu_seqlens, args.n_seqs, total, last_pos, last_start, last_end);
-        walk0.lo_pos = first_start - 1;
-        walk0.hi_pos = args.causal ? last_pos : last_end - 1;
-    }
+    const TileWalk walk0 = unit_walk(args.layout, N, S, q_rank, args.kv_rank_fixed, args.num_steps,
+                                     args.step_base, row0, row_end, args.causal, args.cu_seqlens, args.n_seqs);
 
     // ---- setup
     if (threadIdx.x == 0) {
@@ -671,13 +636,13 @@ __global__ void __launch_bounds__(384, 1)
                 for (int gg = 0; gg < 2; ++gg) {
                     const int fr = row0 + 128 * gg, lrow = min(S, fr + 128) - 1;
                     gvalid[gg] = fr < S;
-                    const int64_t fp = token_pos(args.layout, q_rank, gvalid[gg] ? fr : 0, N, S);
-                    const int64_t lp = token_pos(args.layout, q_rank, gvalid[gg] ? lrow : 0, N, S);
-                    int64_t fs, fe, ls, le;
-                    seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, fp, fs, fe);
-                    seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, lp, ls, le);
-                    glo_pos[gg] = fs - 1;
-                    ghi_pos[gg] = args.causal ? lp : le - 1;
+                    int64_t unused;
+                    row_key_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S,
+                                   token_pos(args.layout, q_rank, gvalid[gg] ? fr : 0, N, S), args.causal,
+                                   glo_pos[gg], unused);
+                    row_key_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S,
+                                   token_pos(args.layout, q_rank, gvalid[gg] ? lrow : 0, N, S), args.causal,
+                                   unused, ghi_pos[gg]);
                 }
                 for (int s0 = 0; s0 < args.num_steps; s0 += 32) {
                     const int st = s0 + lane;
@@ -685,21 +650,12 @@ __global__ void __launch_bounds__(384, 1)
                     if (st < args.num_steps) {
                         const int j = walk0.kv_fixed >= 0 ? walk0.kv_fixed
                                                           : ((q_rank - st - walk0.step_base) % N + N) % N;
-                        const int ulo = (int)(keys_upto(args.layout, j, walk0.lo_pos, N, S) / 128);
-                        const int uhi =
-                            max(ulo, (int)((keys_upto(args.layout, j, walk0.hi_pos, N, S) + 127) / 128));
-                        int e[6] = {ulo, uhi, ulo, ulo, ulo, ulo};
-#pragma unroll
-                        for (int gg = 0; gg < 2; ++gg)
-                            if (gvalid[gg]) {
-                                const int lo = (int)(keys_upto(args.layout, j, glo_pos[gg], N, S) / 128);
-                                const int hi = (int)((keys_upto(args.layout, j, ghi_pos[gg], N, S) + 127) / 128);
-                                e[2 + 2 * gg] = max(lo, ulo);
-                                e[3 + 2 * gg] = max(e[2 + 2 * gg], min(hi, uhi));
-                            }
+                        int e[6];
+                        step_tile_ranges(args.layout, N, S, j, walk0.lo_pos, walk0.hi_pos, glo_pos, ghi_pos,
+                                         gvalid, e);
 #pragma unroll
                         for (int c = 0; c < 6; ++c) step_tab[6 * st + c] = e[c];
-                        cnt = uhi - ulo;
+                        cnt = e[1] - e[0];
                     }
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -734,10 +690,8 @@ __global__ void __launch_bounds__(384, 1)
         float m_ref = 0.f;        // reference point of the exponentials (log2 units)
         float l = 0.f;            // running denominator, relative to m_ref
         float lr = 0.f;           // the same sum over the bf16-rounded P the MMA uses
-        int64_t my_start, my_end;
-        seq_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, my_pos, my_start, my_end);
-        const int64_t my_lo_pos = my_start - 1;
-        const int64_t my_hi_pos = args.causal ? my_pos : my_end - 1;
+        int64_t my_lo_pos, my_hi_pos;
+        row_key_bounds(args.cu_seqlens, args.n_seqs, (int64_t)N * S, my_pos, args.causal, my_lo_pos, my_hi_pos);
         TileWalk w = walk0;
         w.start_step();
         int t = 0;              // key tiles this Q tile has processed
@@ -953,9 +907,9 @@ __global__ void __launch_bounds__(384, 1)
         named_barrier_sync(1 + g, 128);
         if (wq == 0 && lane == 0 && *abort_flag == 0) {
             // rows past the shard's end fall outside the tensor and are not written
-#pragma unroll
             int c1, c2, c3;
             tile_coords(args.seq_order, args.layout, args.S, args.N, ring ? qi : 0, b, row0 + 128 * g, c1, c2, c3);
+#pragma unroll
             for (int bx = 0; bx < NBOX; ++bx) tma_store_4d(&tmo, box_addr(bx), h * D + bx * CPB, c1, c2, c3);
             tma_store_commit();
             tma_store_wait_read();

@@ -46,46 +46,58 @@ ra_status scratch_address(void **out) {
     return RA_OK;
 }
 
+// Bytes of scratch a problem needs: the status word's 256-byte header, then
+// one fp32 partial O [N, B, S, H, d] and LSE [N, B, H, S], each rounded up to
+// 256 bytes; 0 when it cannot fit (the caller has checked the sizes, so the
+// products below cannot overflow once a shard is known to fit).
+size_t scratch_need(int64_t B, int64_t L, int64_t H, int d, int N) {
+    const int64_t S = L / N;
+    if (S * H * (d + 1) * 4 > (int64_t)kNoAllocScratchBytes) return 0;
+    const size_t n_lse = (size_t)N * (size_t)B * (size_t)S * (size_t)H;   // <= 2^30 * 2^24
+    const size_t n_o = n_lse * (size_t)d;
+    const size_t need = kHeaderBytes + round256(n_o * 4) + round256(n_lse * 4);
+    return need <= kNoAllocScratchBytes ? need : 0;
+}
+
 }  // namespace
 
 extern "C" ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void *k, const void *v,
                                                         float *o, float *lse, int64_t B, int64_t L,
                                                         int64_t H, int d, int N, int layout,
-                                                        int causal, float scale, void *stream) {
-    // the same argument checks as ra_ring_attn_fwd
+                                                        int causal, float scale, unsigned flags,
+                                                        void *stream) {
+    // the argument checks of ra_ring_attn_fwd, range limits included
+    if (flags & ~RA_FLAG_INJECT_STALL) return ra::set_error(RA_ERR_INVALID_ARG, "unknown flag bits");
     if (N < 1) return ra::set_error(RA_ERR_SHAPE, "N (ring degree) must be at least 1");
-    if (B < 0 || L < 0 || H < 0) return ra::set_error(RA_ERR_SHAPE, "sizes must be non-negative");
-    if (layout != RA_CONTIGUOUS && layout != RA_STRIPED && layout != RA_ZIGZAG)
-        return ra::set_error(RA_ERR_INVALID_ARG, "unknown layout");
+    if (L < 0) return ra::set_error(RA_ERR_SHAPE, "L must be non-negative");
     if (L % N) return ra::set_error(RA_ERR_SHAPE, "N must divide L");
     if (layout == RA_ZIGZAG && (L % (2 * (int64_t)N)))
         return ra::set_error(RA_ERR_SHAPE, "zigzag needs 2N | L");
-    if (d != 64 && d != 128) return ra::set_error(RA_ERR_UNSUPPORTED, "head dimension d must be 64 or 128");
-    if (!(scale == scale) || scale - scale != 0.f) return ra::set_error(RA_ERR_INVALID_ARG, "scale must be finite");
-    if (B * L * H == 0) return RA_OK;
     const int64_t S = L / N;
-    const size_t n_o = (size_t)B * (size_t)L * (size_t)H * (size_t)d;
-    const size_t n_lse = (size_t)B * (size_t)L * (size_t)H;
-    const size_t o_part_off = kHeaderBytes;
-    const size_t lse_part_off = o_part_off + round256(n_o * 4);
-    const size_t need = lse_part_off + round256(n_lse * 4);
-    if (need > kNoAllocScratchBytes)
+    ra_status st = ra::check_attn_sizes(B, S, H, d, N, layout, scale);
+    if (st != RA_OK) return st;
+    if (B * L * H == 0) return RA_OK;
+    const size_t need = scratch_need(B, L, H, d, N);
+    if (need == 0)
         return ra::set_error(RA_ERR_UNSUPPORTED,
                              "problem needs more scratch than the 64 MiB array of "
-                             "ra_ring_attn_fwd_stepwise_noalloc (B*L*H*(d+1)*4 bytes + 256)");
+                             "ra_ring_attn_fwd_stepwise_noalloc (256 + round256(B*L*H*d*4) + "
+                             "round256(B*L*H*4) bytes)");
     if (!q || !k || !v || !o || !lse) return ra::set_error(RA_ERR_INVALID_ARG, "null pointer argument");
     auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!al(q) || !al(k) || !al(v) || !al(o) || !al(lse))
         return ra::set_error(RA_ERR_ALIGNMENT, "every pointer must be 16-byte aligned");
 
     void *base = nullptr;
-    ra_status st = scratch_address(&base);
+    st = scratch_address(&base);
     if (st != RA_OK) return st;
     uint8_t *scratch = static_cast<uint8_t *>(base);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the status word starts every call at zero; the partials are rewritten in full by every step
-    if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), s) != cudaSuccess)
-        return ra::set_error(RA_ERR_CUDA, "clearing the scratch status word failed");
+    // The status word is not cleared here: it collects the timeouts of every
+    // call until ra_noalloc_check_status reads and clears it (it is zero when
+    // the library is loaded).  The partials are rewritten in full by every step.
+    const size_t o_part_off = kHeaderBytes;
+    const size_t lse_part_off = o_part_off + round256((size_t)N * B * S * H * d * 4);
 
     ra::AttnLaunch a{};
     a.q = q;
@@ -107,6 +119,7 @@ extern "C" ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void
     const char *err = nullptr;
     for (int step = 0; step < N; ++step) {
         a.ring_step = step;
+        a.inject_stall = step == 0 && (flags & RA_FLAG_INJECT_STALL) != 0;
         a.o = step == 0 ? static_cast<void *>(o) : static_cast<void *>(o_part);
         a.lse = step == 0 ? lse : lse_part;
         st = ra::launch_attention(a, s, &err);
@@ -117,4 +130,24 @@ extern "C" ra_status ra_ring_attn_fwd_stepwise_noalloc(const void *q, const void
         }
     }
     return RA_OK;
+}
+
+extern "C" ra_status ra_noalloc_check_status(void *stream) {
+    void *base = nullptr;
+    ra_status st = scratch_address(&base);
+    if (st != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return ra::set_error(RA_ERR_CUDA, "cudaStreamSynchronize failed");
+    if (cudaMemcpy(&word, base, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ra::set_error(RA_ERR_CUDA, "reading the scratch status word failed");
+    if (word == 0) return RA_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpy(base, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return ra::set_error(RA_ERR_CUDA, "clearing the scratch status word failed");
+    if (word & ra::RA_DEV_TIMEOUT_BIT)
+        return ra::set_error(RA_ERR_TIMEOUT, "a kernel of the allocation-free sweep gave up on a bounded wait");
+    return ra::set_error(RA_ERR_ALIGNMENT,
+                         "a kernel of the allocation-free sweep found its shared memory base unaligned");
 }

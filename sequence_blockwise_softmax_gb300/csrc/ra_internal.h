@@ -40,9 +40,8 @@ struct AttnLaunch {
 ra_status launch_attention(const AttnLaunch &a, cudaStream_t stream, const char **err);
 
 // Bytes of streamed operands per chunk of (batch, head) pairs whose units a
-// launch interleaves heaviest first (see the kernels' unit decode): the
-// RA_L2_CHUNK_KB environment variable if set to a positive number, read at
-// every launch, else 48 MiB.
+// launch interleaves heaviest first (decode_unit): 48 MiB, or what
+// ra_set_launch_chunk_budget last set.
 int64_t l2_chunk_bytes();
 
 // Pairs per chunk for `per_pair` streamed bytes each, between 1 and `pairs`
@@ -79,9 +78,14 @@ ra_status launch_permute(const void *src, void *dst, int op, int layout, int64_t
 ra_status launch_lse_to_seq(const float *src, float *dst, int layout, int64_t B, int64_t L,
                             int64_t H, int R, int U, cudaStream_t stream, const char **err);
 
+// O [B, S, H, d] and LSE [B, H, S] (the ring calls' tensors)
 ra_status launch_lse_merge(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
                            int64_t B, int64_t S, int64_t H, int d, cudaStream_t stream,
                            const char **err);
+// `rows` rows: O row r at o + r * row_stride (floats), its LSE at lse[r]
+ra_status launch_lse_merge_rows(float *o_acc, float *lse_acc, const float *o_b, const float *lse_b,
+                                int64_t rows, int d, int64_t acc_row_stride, int64_t b_row_stride,
+                                cudaStream_t stream, const char **err);
 
 // fp32 -> bf16 copy of n elements (n a multiple of 4): the stepwise ring finish
 ra_status launch_f32_to_bf16(const float *src, void *dst, int64_t n, cudaStream_t stream,
@@ -121,5 +125,11 @@ inline TileView tile_view(bool seq_order, int layout, int64_t S, int64_t B, int6
 
 // Record `msg` as this host thread's ra_last_error() text and return `st`.
 ra_status set_error(ra_status st, const char *msg);
+
+// The host-side range checks every attention entry point applies to a ring or
+// block problem of shard length S (the sizes the kernels index with 32-bit
+// ints and the tensor maps' stride limit); RA_OK or the failing status, with
+// the message recorded.
+ra_status check_attn_sizes(int64_t B, int64_t S, int64_t H, int d, int N, int layout, float scale);
 
 }  // namespace ra

@@ -71,7 +71,8 @@ def test_empty_inputs_are_no_ops(ralib):
     assert _ring(ralib, L=0, q=0, k=0, v=0, o=0, lse=0, ws=0) == 0
     lib = ralib.lib()
     assert lib.ra_shard_permute(None, None, 0, 0, 0, 16, 2, 64, 4, 1, 2, None) == 0
-    assert lib.ra_lse_merge(None, None, None, None, 1, 0, 2, 64, None) == 0
+    assert lib.ra_lse_merge_bshd(None, None, None, None, 1, 0, 2, 64, None) == 0
+    assert lib.ra_lse_merge(None, None, None, None, 0, 64, 64, 64, None) == 0
 
 
 def test_permute_rejects_bad_arguments(ralib):
@@ -134,12 +135,12 @@ def test_workspace_sizes(ralib):
     assert ralib.ra_ring_attn_workspace_bytes(1, 1024, 2, 96, 4, 0) == 0
 
 
-def test_launch_chunk_pairs(ralib, monkeypatch):
+def test_launch_chunk_pairs(ralib):
     """The launch-order chunk: all pairs when they stream at most 5/3 of the
     budget together, else the fewest near-equal chunks of at most the budget
-    (48 MiB, or RA_L2_CHUNK_KB), clamped to [1, pairs]."""
+    (48 MiB, or what ra_set_launch_chunk_budget set), clamped to [1, pairs]."""
     MiB = 1 << 20
-    monkeypatch.delenv("RA_L2_CHUNK_KB", raising=False)
+    assert ralib.ra_set_launch_chunk_budget(0) == 48 * MiB     # the default, and it is restored
     assert ralib.ra_launch_chunk_pairs(4 * MiB, 16) == 16      # config 2: 64 MiB in all, one chunk
     assert ralib.ra_launch_chunk_pairs(6 * MiB, 16) == 8       # 96 MiB > 5/3 budget: 8 fit, so 8 + 8
     assert ralib.ra_launch_chunk_pairs(16 * MiB, 64) == 3      # config 3: 3 per chunk
@@ -148,12 +149,73 @@ def test_launch_chunk_pairs(ralib, monkeypatch):
     assert ralib.ra_launch_chunk_pairs(1 * MiB, 8) == 8
     assert ralib.ra_launch_chunk_pairs(0, 8) == 1
     assert ralib.ra_launch_chunk_pairs(MiB, 0) == 0
+    try:
+        assert ralib.ra_set_launch_chunk_budget(MiB) == 48 * MiB
+        assert ralib.ra_launch_chunk_pairs(512 * 1024, 5) == 2     # 2 + 2 + 1
+        assert ralib.ra_launch_chunk_pairs(512 * 1024, 3) == 3     # 1.5 MiB <= 5/3 MiB: one chunk
+        for bad in (0, -5):                                        # back to the default
+            assert ralib.ra_set_launch_chunk_budget(bad) in (MiB, 48 * MiB)
+            assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3, bad
+    finally:
+        ralib.ra_set_launch_chunk_budget(0)
+
+
+def test_no_environment_knob(ralib, monkeypatch):
+    """The launch order reads nothing from the environment."""
+    MiB = 1 << 20
     monkeypatch.setenv("RA_L2_CHUNK_KB", "1024")
-    assert ralib.ra_launch_chunk_pairs(512 * 1024, 5) == 2     # 2 + 2 + 1
-    assert ralib.ra_launch_chunk_pairs(512 * 1024, 3) == 3     # 1.5 MiB <= 5/3 MiB: one chunk
-    for bad in ("0", "-5", "abc", ""):
-        monkeypatch.setenv("RA_L2_CHUNK_KB", bad)
-        assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3, bad
+    assert ralib.ra_launch_chunk_pairs(16 * MiB, 8) == 3
+
+
+def test_merge_rejects_bad_arguments(ralib):
+    lib = ralib.lib()
+    M = lambda rows, d, sa, sb, oa=FAKE, la=FAKE: lib.ra_lse_merge(oa, la, FAKE + 4096, FAKE + 8192, rows, d,
+                                                                   sa, sb, None)
+    assert M(10, 6, 8, 8) == 3              # d not a multiple of 4
+    assert M(10, 260, 260, 260) == 3        # d above 256
+    assert M(10, 64, 60, 64) == 2           # rows would overlap
+    assert M(10, 64, 66, 64) == 4           # stride not a multiple of 4 floats
+    assert M(10, 64, 64, 64, oa=0) == 1     # null
+    assert M(10, 64, 64, 64, oa=FAKE + 4) == 4
+    assert M(10, 64, 64, 64, la=FAKE + 2) == 4
+    assert M(-1, 64, 64, 64) == 2
+    assert lib.ra_lse_merge_bshd(FAKE, FAKE + 4, FAKE, FAKE, 1, 8, 2, 64, None) == 4
+
+
+NOALLOC_CAP = 64 << 20
+
+
+def _noalloc_need(B, L, H, d):
+    r256 = lambda x: (x + 255) // 256 * 256
+    return 256 + r256(B * L * H * d * 4) + r256(B * L * H * 4)
+
+
+def test_noalloc_limit_at_the_boundary(ralib):
+    """The stated limit 256 + round256(B*L*H*d*4) + round256(B*L*H*4) <= 64 MiB: a problem
+    needing exactly 64 MiB passes the size check (here, without a GPU, it then fails at the
+    device lookup), one token more is rejected as too large."""
+    lib = ralib.lib()
+    assert _noalloc_need(1, 26011, 5, 128) == NOALLOC_CAP
+    assert _noalloc_need(1, 26012, 5, 128) > NOALLOC_CAP
+    call = lambda L, flags=0: lib.ra_ring_attn_fwd_stepwise_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, L, 5, 128, 1,
+                                                                    0, 1, 0.0, flags, None)
+    import torch
+    if not torch.cuda.is_available():
+        assert call(26011) == 5                      # past the checks: no device to look up
+    assert call(26012) == 3
+    assert "64 MiB" in lib.ra_last_error().decode()
+    assert call(26011, flags=1) == 1                 # only the stall hook is a valid flag
+
+
+def test_noalloc_applies_the_range_checks(ralib):
+    """Sizes whose products would wrap around are rejected by the same range checks as
+    ra_ring_attn_fwd before any scratch arithmetic."""
+    lib = ralib.lib()
+    big = lambda B, L, H: lib.ra_ring_attn_fwd_stepwise_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, B, L, H, 128, 1,
+                                                                 0, 1, 0.0, 0, None)
+    assert big(1 << 21, 1 << 20, 1 << 21) == 3     # B*L*H = 2^62: would wrap the byte count to 0
+    assert big(1, 1 << 20, 1 << 21) == 3
+    assert big(1 << 21, 16, 1) == 3
 
 
 def _bwd(ralib, **kw):

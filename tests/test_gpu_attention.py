@@ -169,7 +169,7 @@ def test_block_steps_merge_to_full(ralib, gpu):
             ralib.ra_block_attn_fwd(sh[0][i], sh[1][j], sh[2][j], dst_o, dst_l, B, S, H, d, N, i, j,
                                     layout, True, workspace=ws)
             if step:
-                ralib.ra_lse_merge(acc_o, acc_l, part_o, part_l, B, S, H, d)
+                ralib.ra_lse_merge_bshd(acc_o, acc_l, part_o, part_l, B, S, H, d)
         o_seq[:, pos[i]] = acc_o.cpu().numpy()
         lse_seq[:, :, pos[i]] = acc_l.cpu().numpy()
     o_ref, lse_ref = oracle.full_attention(q, k, v, causal=True)

@@ -4,7 +4,7 @@ Causal work grows with position, so the forward and both backward passes run
 heavy units first, taking (batch, head) pairs in chunks whose keys and values
 fit in L2 together ("From Ring Attention to DeepSpeed Ulysses to USP",
 jsqmd.com/news/734632, §3.4 and §4 discuss the causal imbalance this evens
-out on one device).  RA_L2_CHUNK_KB sets the chunk budget.  Here it is set so
+out on one device).  ra_set_launch_chunk_budget sets the chunk budget.  Here it is set so
 that the chunks split the pairs unevenly (a partial last chunk), and the results
 must be bit-identical to those of the default order -- every unit's arithmetic
 is independent of when it runs -- and match the fp64 oracle.
@@ -34,21 +34,24 @@ CASES = [
 
 
 @pytest.mark.parametrize("B,L,H,Hkv,d,N,layout,kb", CASES)
-def test_chunked_order_bit_identical(ralib, gpu, monkeypatch, B, L, H, Hkv, d, N, layout, kb):
+def test_chunked_order_bit_identical(ralib, gpu, B, L, H, Hkv, d, N, layout, kb):
     ra = ralib
     seed = 7000 + L + H
     q, k, v = randn_bf16((B, L, H, d), seed), randn_bf16((B, L, Hkv, d), seed + 1), randn_bf16((B, L, Hkv, d), seed + 2)
     do = randn_bf16((B, L, H, d), seed + 3)
-    monkeypatch.delenv("RA_L2_CHUNK_KB", raising=False)
+    ra.ra_set_launch_chunk_budget(0)
     o0, lse0 = run_ring_gqa(ra, q, k, v, N, layout, True)
     g0 = run_bwd(ra, q, k, v, do, N, layout, True)
-    monkeypatch.setenv("RA_L2_CHUNK_KB", str(kb))
-    # the forward's and the dQ pass's chunks split the pairs unevenly
-    group = H // Hkv
-    c = ra.ra_launch_chunk_pairs(4 * L * d // group, B * H)
-    assert 1 < c < B * H and (B * H) % c != 0, c
-    o1, lse1 = run_ring_gqa(ra, q, k, v, N, layout, True)
-    g1 = run_bwd(ra, q, k, v, do, N, layout, True)
+    ra.ra_set_launch_chunk_budget(kb << 10)
+    try:
+        # the forward's and the dQ pass's chunks split the pairs unevenly
+        group = H // Hkv
+        c = ra.ra_launch_chunk_pairs(4 * L * d // group, B * H)
+        assert 1 < c < B * H and (B * H) % c != 0, c
+        o1, lse1 = run_ring_gqa(ra, q, k, v, N, layout, True)
+        g1 = run_bwd(ra, q, k, v, do, N, layout, True)
+    finally:
+        ra.ra_set_launch_chunk_budget(0)
     assert np.array_equal(o0, o1) and np.array_equal(lse0, lse1), "forward depends on the unit order"
     for a, b, name in zip(g0, g1, ("dq", "dk", "dv")):
         assert np.array_equal(a, b), name + " depends on the tile order"
