@@ -22,7 +22,7 @@
 //               of three shared-memory slots, K a tile ahead of V.
 //   warp 1      MMA issuer (one elected lane): S_g = Q_g K^T into tensor
 //               memory, and at d = 64 also O_g += P_g V with P_g read from
-//               shared memory.
+//               tensor memory.
 //   warp 2      tensor-memory allocator.
 //   warp 3      at d = 128, the PV issuer, so that a wait of either issuer
 //               never holds back the other's products (the tensor pipe takes
@@ -30,12 +30,15 @@
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
 //               query row (the 32x32b tensor-memory load gives a thread its
 //               whole row, so row sums need no shuffles), exp2 with the
-//               scale folded into log2(e), P written to shared memory as
-//               bf16, O rescaled in place when the reference point moves,
+//               scale folded into log2(e), P written as bf16 to shared memory
+//               (d = 128) or tensor memory (d = 64), O rescaled in place when
+//               the reference point moves,
 //               and the final normalisation, with O staged in shared memory
 //               for TMA stores.
 // Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
-// O_0 [256, 256+d), O_1 [256+d, 256+2d).  Because P does not live in S's
+// O_0 [256, 256+d), O_1 [256+d, 256+2d), and at d = 64 P_0 [384, 448),
+// P_1 [448, 512) (bf16 pairs), which PV reads from there; at d = 128 P goes
+// through shared memory.  Because P does not live in S's
 // columns, S_g(t+1) may be computed while PV_g(t) still runs: the softmax
 // releases S_g once P is computed and its denominator checked (the rare
 // second pass reloads S), and each tile's critical chain is S -> softmax ->
@@ -170,6 +173,11 @@ __global__ void __launch_bounds__(384, 1)
     // At d = 128 warp 1 issues the S products and warp 3 the PV products; at
     // d = 64, where the split measured slower, warp 1 issues both.
     constexpr bool TWO_ISSUERS = D == 128;
+    // At d = 64 tensor memory has room for P next to S and O (columns 384-511),
+    // so P_g goes there and PV_g reads it as the A operand (a TS product): no
+    // P stores through shared memory and no proxy fence.  At d = 128 S and O
+    // fill all 512 columns and P goes through shared memory.
+    constexpr bool P_IN_TMEM = D == 64;
     // registers per thread of warps 0-3 after setmaxnreg: the second issuer
     // needs more than 64 to issue without spilling
     constexpr uint32_t LOW_REGS = TWO_ISSUERS ? 72u : 64u;
@@ -354,14 +362,27 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint32_t hb = L::kBox >> 4;
             const uint64_t a0 = dp[g], b0 = dv0 + (uint64_t)(slot * (L::kTile >> 4));
             const uint32_t d = tmem + 256 + g * D;
-            mma_ss_elect<0, 0>(d, a0, b0, IDESC_O, first ? 0u : 1u);
-            mma_ss_elect<2, 128>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<4, 256>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<6, 384>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<hb, 512>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<hb + 2, 640>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<hb + 4, 768>(d, a0, b0, IDESC_O, 1u);
-            mma_ss_elect<hb + 6, 896>(d, a0, b0, IDESC_O, 1u);
+            if constexpr (P_IN_TMEM) {
+                // A = P_g in tensor memory: 16 keys (8 packed columns) per k-step
+                const uint32_t at = tmem + 384 + g * 64;
+                mma_ts_elect<0, 0>(d, at, b0, IDESC_O, first ? 0u : 1u);
+                mma_ts_elect<8, 128>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<16, 256>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<24, 384>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<32, 512>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<40, 640>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<48, 768>(d, at, b0, IDESC_O, 1u);
+                mma_ts_elect<56, 896>(d, at, b0, IDESC_O, 1u);
+            } else {
+                mma_ss_elect<0, 0>(d, a0, b0, IDESC_O, first ? 0u : 1u);
+                mma_ss_elect<2, 128>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<4, 256>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<6, 384>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<hb, 512>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<hb + 2, 640>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<hb + 4, 768>(d, a0, b0, IDESC_O, 1u);
+                mma_ss_elect<hb + 6, 896>(d, a0, b0, IDESC_O, 1u);
+            }
             tc_commit_elect(BAR(B_PVDONE + g));
         };
         bool ok = warp_wait(BAR(B_QFULL), 0, abort_flag);
@@ -726,11 +747,22 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
                 tmem_wait_ld();
-                if (partial) {
+                if (__any_sync(0xffffffffu, partial)) {
+                    // the warp's rows see columns [lim_lo, lim) each; a 32-column
+                    // chunk inside [largest lim_lo, smallest lim) is visible to
+                    // every row of the warp and needs no mask (a warp's limits
+                    // differ by about one column per row, so at most two chunks
+                    // of a tile are masked element by element)
+                    const int hi_min = (int)__reduce_min_sync(0xffffffffu, (unsigned)min(max(lim, 0), 128));
+                    const int lo_max = (int)__reduce_max_sync(0xffffffffu, (unsigned)min(max(lim_lo, 0), 128));
                     float *s = reinterpret_cast<float *>(&sr[0][0]);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c >= lim || c < lim_lo) s[c] = -INFINITY;
+                    for (int q = 0; q < 4; ++q) {
+                        if (32 * q >= lo_max && 32 * q + 32 <= hi_min) continue;
+#pragma unroll
+                        for (int c = 32 * q; c < 32 * q + 32; ++c)
+                            if (c >= lim || c < lim_lo) s[c] = -INFINITY;
+                    }
                 }
             };
             // P is computed against the current reference point and kept in
@@ -819,8 +851,21 @@ __global__ void __launch_bounds__(384, 1)
             // P_g(t) goes to shared memory -- the K-major A operand of PV in the
             // 128-byte-swizzled layout a TMA box load would give (16-byte chunk
             // j of row r at chunk j ^ (r mod 8); keys 0-63 in the first box) --
-            // once PV_g(t-1) has read P_g(t-1) there
+            // or, at d = 64, to its tensor-memory columns, once PV_g(t-1) has
+            // read P_g(t-1) there
             if (t > 0 && !(ok = warp_wait(BAR(B_PVDONE + g), (t - 1) & 1, abort_flag))) break;
+            if constexpr (P_IN_TMEM) {
+                // the row's 128 keys as 64 packed columns (key c in the low half
+                // of column c / 2), the layout a TS product reads A in
+                const uint32_t tP = tmem + lane_off + 384 + g * 64;
+                tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(&pr[0][0]));
+                tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pr[2][0]));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR(B_PFULL + g));
+                if constexpr (SKIP) ++t;
+                continue;
+            }
             {
                 // row base (1024-byte aligned group + 128 bytes per row) and the
                 // row's chunk swizzle; both are recomputed every tile rather than
