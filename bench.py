@@ -178,7 +178,7 @@ class ClockSampler:
 # ----------------------------------------------------------------- the GPU path
 class Workload:
     def __init__(self, ra, name, layout, dev, shape=None, stepwise=False, kv_heads=None, varlen=None,
-                 seq_order=True):
+                 seq_order=True, loopback=False):
         w = dict(WORKLOADS[name])
         if shape is not None:
             w.update(B=shape[0], L=shape[1], H=shape[2], d=shape[3], N=shape[4])
@@ -191,8 +191,9 @@ class Workload:
         # token-order sweep (RA_FLAG_SEQ_ORDER): the layout is the tiles' addresses and no
         # permute runs; the Ulysses split, the stepwise sweep and zigzag chunks that are not
         # a multiple of 128 rows take the explicit permutes
-        self.seq_order = (seq_order and U == 1 and not stepwise and
+        self.seq_order = (seq_order and U == 1 and not stepwise and not loopback and
                           not (layout == "zigzag" and (L // N // 2) % 128))
+        self.loopback = loopback
         q, k, v, _ = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])
         if self.Hkv != H:
             # grouped-query attention: the first H_kv heads of the drawn K and V
@@ -233,6 +234,19 @@ class Workload:
         self.launches = 3 * (2 if U > 1 else 1) + attn_launches + (2 if U > 1 else 1) + 1
         if self.seq_order:
             self.launches = 1
+        if loopback:
+            # the multi-GPU ring driver with its N ranks on this GPU (device-to-device
+            # copies on a copy stream in place of the transfers)
+            if U != 1 or varlen:
+                raise ValueError("the loopback ring runs plain ring layouts")
+            from sequence_blockwise_softmax_gb300 import ring
+            self.ring = ring
+            self.ring_ranks = ring.loopback_ranks(*self.shard, N, layout, self.causal, o=self.o_ring,
+                                                  lse=self.lse_ring)
+            self.comm_stream = torch.cuda.Stream(device=dev)
+            active = sum(1 for r in self.ring_ranks for st, j, p in r.schedule if st == 0 or p)
+            self.launches = 3 + (2 * active - N) + 2
+            self.ring_bytes = ring.ring_bytes_per_step(B, L // N, self.Hkv, d) * N * (N - 1)
         self.attn_events = []
 
     def step(self, time_attention=False, slot=0):
@@ -263,7 +277,9 @@ class Workload:
         if time_attention:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-        if self.cu is not None:
+        if self.loopback:
+            self.ring.run_ring(self.ring_ranks, self.ring.LoopbackRing(), self.comm_stream)
+        elif self.cu is not None:
             ra.ra_ring_attn_fwd_varlen(*ring_in, self.o_ring, self.lse_ring, self.cu, L, H, self.Hkv, d, N,
                                        self.layout, self.causal, flags=self.flags, workspace=self.ws)
         elif self.Hkv == H:
@@ -571,6 +587,10 @@ def main():
     ap.add_argument("--explicit-permutes", action="store_true",
                     help="run the forward on shard stacks with the permute kernels around the sweep "
                          "instead of the token-order sweep")
+    ap.add_argument("--ring-loopback", action="store_true",
+                    help="run the multi-GPU ring driver (sequence_blockwise_softmax_gb300.ring) with its N ranks "
+                         "on this GPU: per rank and step a block call and a merge, the K/V shift as "
+                         "device-to-device copies on a copy stream")
     ap.add_argument("--varlen", type=int, default=None,
                     help="pack this many variable-length sequences (seeded cut points) into the workload")
     ap.add_argument("--kv-heads", type=int, default=None,
@@ -598,7 +618,7 @@ def main():
     layout = args.layout or w["layouts"][0]
     shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
     wl = Workload(ra, args.workload, layout, dev, shape, stepwise=args.stepwise, kv_heads=args.kv_heads,
-                  varlen=args.varlen, seq_order=not args.explicit_permutes)
+                  varlen=args.varlen, seq_order=not args.explicit_permutes, loopback=args.ring_loopback)
 
     step = wl.step
     if args.backward:
@@ -635,7 +655,7 @@ def main():
     peak_sustained = float(peaks.get("bf16_tflops_sustained", peak))
     achieved = wl.flops / (attn_ms * 1e-3) / 1e12
     # the committed DRAM figure is for the default forward launch only
-    default_launch = not (args.backward or args.stepwise or args.varlen or args.kv_heads or shape
+    default_launch = not (args.backward or args.stepwise or args.ring_loopback or args.varlen or args.kv_heads or shape
                           or args.workload != DEFAULT_WORKLOAD or layout != "striped")
     traffic = read_traffic() if default_launch else None
 
@@ -647,7 +667,8 @@ def main():
                    "d": wl.d, "N": wl.N, "U": wl.U, "H_kv": wl.Hkv, "causal": wl.causal,
                    "packed_sequences": args.varlen,
                    "parallelism": "replicas" if world > 1 else "single GPU, %d virtual ranks" % wl.N,
-                   "sweep": "stepwise" if args.stepwise else "fused",
+                   "sweep": ("ring driver, N ranks on one GPU (loopback transfers)" if args.ring_loopback
+                             else "stepwise" if args.stepwise else "fused"),
                    "io": ("token order: the layout is the sweep's tile addressing, no permute kernels"
                           if wl.seq_order else "shard stacks with explicit permute kernels"),
                    "l2": "inputs larger than L2 (q/k/v %.0f MiB)" % (wl.h2d_bytes() / 2 ** 20)},
@@ -655,6 +676,8 @@ def main():
                      "frac": achieved / peak, "frac_of_sustained": achieved / peak_sustained,
                      "traffic": traffic,
                      "kernel": ("ra_ring_attn_bwd: bwd_dot + attn_bwd_dkv + attn_bwd_dq" if args.backward else
+                                "ring driver: per rank and step attn_fwd_kernel<fp32 partial> + lse_merge_kernel, "
+                                "K/V copies on a copy stream" if args.ring_loopback else
                                 "ra_ring_attn_fwd stepwise: N x attn_fwd_kernel<fp32 partial> + N-1 x lse_merge_kernel"
                                 if args.stepwise else "attn_fwd_kernel<128, fp32 O> (ra_ring_attn_fwd)"),
                      "kernel_ms": attn_ms,
@@ -668,6 +691,12 @@ def main():
         "clocks": clocks.summary(),
     }
 
+    if args.ring_loopback:
+        per = wl.ring.ring_bytes_per_step(wl.B, wl.L // wl.N, wl.Hkv, wl.d)
+        line["ring_driver"] = {
+            "bytes_per_rank_step": per, "copy_bytes_per_sweep": per * wl.N * (wl.N - 1),
+            "transport": "device-to-device copies on a copy stream (one GPU holds all ranks); on N GPUs "
+                         "the same driver moves these bytes with NCCL point-to-point (not measured here)"}
     if wl.cu is None:
         bal = balance_table(layout, wl.N, wl.L // wl.N, wl.causal)
         if args.stepwise:
