@@ -454,11 +454,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             const uint32_t tSb = tS + s_col(t);
             const int lim = khi - w.tile * 128, lim_lo = klo - w.tile * 128;
-            // a 32-column chunk inside [largest lim_lo, smallest lim) of the warp
-            // is visible to all its rows and needs no mask (warp-uniform test)
-            const bool partial = __any_sync(0xffffffffu, lim < 128 || lim_lo > 0);
-            const int hi_min = (int)__reduce_min_sync(0xffffffffu, (unsigned)min(max(lim, 0), 128));
-            const int lo_max = (int)__reduce_max_sync(0xffffffffu, (unsigned)min(max(lim_lo, 0), 128));
+            const bool partial = lim < 128 || lim_lo > 0;
             const uint64_t sl2x2 = f32x2(sl2, sl2), nl2 = f32x2(-lse2, -lse2), dd2 = f32x2(dval, dval);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -466,7 +462,7 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t sv[32], out[16];
                 tmem_ld32(tSb + c0, sv);
                 tmem_wait_ld();
-                if (partial && !(c0 >= lo_max && c0 + 32 <= hi_min)) {
+                if (partial) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         if (c0 + c >= lim || c0 + c < lim_lo) sv[c] = __float_as_uint(-INFINITY);
@@ -802,21 +798,14 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive(BAR(B_SFREE));
             // masked queries get S = -inf (P = 0) in a loop of their own, so the
             // exponential loop below stays one block the compiler can schedule
-            // (a 32-column chunk inside [largest lim_lo, smallest lim) of the
-            // warp is visible to all its rows: warp-uniform test)
-            if (__any_sync(0xffffffffu, lim < 128 || lim_lo > 0)) {
-                const int hi_min = (int)__reduce_min_sync(0xffffffffu, (unsigned)min(max(lim, 0), 128));
-                const int lo_max = (int)__reduce_max_sync(0xffffffffu, (unsigned)min(max(lim_lo, 0), 128));
+            if (lim < 128 || lim_lo > 0) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = 64 * hh + 32 * j;
-                    if (c0 >= lo_max && c0 + 32 <= hi_min) continue;
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const int col = c0 + c;
+                        const int col = 64 * hh + 32 * j + c;
                         if (col >= lim || col < lim_lo) pv[j][c] = __float_as_uint(-INFINITY);
                     }
-                }
             }
             const uint64_t sl2x2 = f32x2(sl2, sl2);
             // P^T stays in registers only as the packed bf16 the dV product uses

@@ -11,6 +11,9 @@
 #include "ra_internal.h"
 
 #define RA_HD __host__ __device__ __forceinline__
+// the walks' step changes: left to the compiler to inline or not, to keep the
+// kernels' per-tile loops short
+#define RA_HD_STEP __host__ __device__
 
 namespace ra {
 
@@ -77,7 +80,7 @@ struct TileWalk {
     int num_steps, step_base, q_rank, kv_fixed, N, layout, S;
     int64_t lo_pos, hi_pos;
 
-    RA_HD void start_step() {
+    RA_HD_STEP void start_step() {
         while (step < num_steps) {
             j = kv_fixed >= 0 ? kv_fixed : ((q_rank - step - step_base) % N + N) % N;
             const int64_t lo = keys_upto(layout, j, lo_pos, N, S);
@@ -88,8 +91,8 @@ struct TileWalk {
             ++step;
         }
     }
-    RA_HD bool valid() const { return step < num_steps; }
-    RA_HD void next() {
+    RA_HD_STEP bool valid() const { return step < num_steps; }
+    RA_HD_STEP void next() {
         if (++tile >= tile_end) {
             ++step;
             start_step();
@@ -144,7 +147,7 @@ struct QWalk {
     int heads, N, j, layout, S;
     int64_t lo_pos, hi_pos;
 
-    RA_HD void start() {
+    RA_HD_STEP void start() {
         while (head < heads) {
             while (step < N) {
                 i = (j + step) % N;
@@ -159,8 +162,8 @@ struct QWalk {
             ++head;
         }
     }
-    RA_HD bool valid() const { return head < heads; }
-    RA_HD void next() {
+    RA_HD_STEP bool valid() const { return head < heads; }
+    RA_HD_STEP void next() {
         if (++tile >= tile_end) {
             ++step;
             start();
