@@ -32,9 +32,17 @@ RA_HD int64_t clamp64(int64_t x, int64_t lo, int64_t hi) {
 
 // How many keys of rank j sit at global positions <= p.  Because positions
 // increase along a rank's local order, these are local keys 0..result-1.
+// (The striped quotient is taken in 32 bits whenever it fits: a 64-bit
+// division is several times longer, and the kernels evaluate this at every
+// ring step of every row.)
 RA_HD int64_t keys_upto(int layout, int j, int64_t p, int N, int64_t S) {
     if (layout == RA_CONTIGUOUS) return clamp64(p - (int64_t)j * S + 1, 0, S);
-    if (layout == RA_STRIPED) return p < j ? 0 : (((p - j) / N + 1) < S ? (p - j) / N + 1 : S);
+    if (layout == RA_STRIPED) {
+        if (p < j) return 0;
+        const int64_t q = p - j;
+        const int64_t n = q <= 0x7fffffffLL ? (int64_t)((uint32_t)q / (uint32_t)N) + 1 : q / N + 1;
+        return n < S ? n : S;
+    }
     const int64_t C = S >> 1;
     return clamp64(p - (int64_t)j * C + 1, 0, C) + clamp64(p - (int64_t)(2 * N - 1 - j) * C + 1, 0, C);
 }
