@@ -110,3 +110,33 @@ def test_backward_full_size(ralib, gpu, Hkv):
                      for h in range(kv * group, (kv + 1) * group)]
             assert_grad_close(dk_tail[b, :, kv], sum(p[1] for p in parts)[k0:], "dK last keys, kv head %d" % kv)
             assert_grad_close(dv_tail[b, :, kv], sum(p[2] for p in parts)[k0:], "dV last keys, kv head %d" % kv)
+
+
+def test_backward_zigzag_32k_whole_head(ralib, gpu):
+    """Every gradient element of one (batch, head) of the 2 x 32K zigzag workload (H = 32,
+    N = 8, 1 % of the key rows scaled x4), through the token-order backward, against the
+    fp64 derivative computed over all rows of that head: dQ of every row, and dK and dV of
+    every key as the sum of all rows' contributions."""
+    w = WORKLOADS["zigzag_B2_H32_L32768_d128_N8_kscaled"]
+    B, L, H, d, N = w["B"], w["L"], w["H"], w["d"], w["N"]
+    q, k, v, _ = make_qkv(B, L, H, d, w["seed"], w["k_scale_frac"])
+    do = make_dout(B, L, H, d, seed=11)
+    dev = torch.device("cuda:0")
+    qg, kg, vg, dog = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    flags = ralib.RA_FLAG_SEQ_ORDER
+    o = torch.empty((B, L, H, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    ws = ralib.new_workspace(max(ralib.ra_ring_attn_workspace_bytes(B, L, H, d, N, flags),
+                                 ralib.ra_ring_attn_bwd_workspace_bytes(B, L, H, d, N)))
+    ralib.ra_ring_attn_fwd(qg, kg, vg, o, lse, B, L, H, d, N, "zigzag", True, flags=flags, workspace=ws)
+    dq = torch.empty_like(o)
+    dk = torch.empty_like(o)
+    dv = torch.empty_like(o)
+    ralib.ra_ring_attn_bwd(qg, kg, vg, o, dog, lse, dq, dk, dv, B, L, H, H, d, N, "zigzag", True, workspace=ws,
+                           flags=flags)
+    ralib.ra_check_status(ws)
+    b, h = 1, 7
+    ref_dq, ref_dk, ref_dv = attention_backward_rows(q, k, v, do, True, b, h, np.arange(L), chunk=256)
+    assert_grad_close(dq[b, :, h].cpu().numpy(), ref_dq, "dQ, zigzag 32K, every row")
+    assert_grad_close(dk[b, :, h].cpu().numpy(), ref_dk, "dK, zigzag 32K, every key")
+    assert_grad_close(dv[b, :, h].cpu().numpy(), ref_dv, "dV, zigzag 32K, every key")

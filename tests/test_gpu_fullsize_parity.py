@@ -169,3 +169,31 @@ def test_128k_block_calls(ralib, gpu, q_rank, kv_rank):
                                             q_rank, kv_rank, True)
     assert_attention_close(o.cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref,
                            "128K block q_rank %d kv_rank %d" % (q_rank, kv_rank))
+
+
+@pytest.mark.parametrize("layout", ["striped", "zigzag"])
+def test_32k_gqa_and_packed_whole_heads(ralib, gpu, layout):
+    """Grouped key/value heads (H = 8, H_kv = 2) with 48 packed sequences over 32K tokens,
+    N = 8, token order: in the striped layout this runs the tile-skipping kernel variant.
+    Two whole query heads (of different key/value heads), every row, element by element."""
+    B, L, H, Hkv, d, N = 1, 32768, 8, 2, 128, 8
+    from synthetic_inputs import make_cu_seqlens, randn_bf16
+    q = randn_bf16((B, L, H, d), 8101)
+    k = randn_bf16((B, L, Hkv, d), 8102)
+    v = randn_bf16((B, L, Hkv, d), 8103)
+    cu = make_cu_seqlens(L, 48, seed=8104).numpy()
+    dev = torch.device("cuda:0")
+    cu_dev = torch.as_tensor(cu, dtype=torch.int32, device=dev)
+    o = torch.empty((B, L, H, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    flags = ralib.RA_FLAG_SEQ_ORDER
+    ws = ralib.new_workspace(ralib.ra_ring_attn_workspace_bytes(B, L, H, d, N, flags))
+    ralib.ra_ring_attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), o, lse, cu_dev, L, H, Hkv, d, N, layout, True,
+                                  flags=flags, workspace=ws)
+    ralib.ra_check_status(ws)
+    for h in (1, 6):
+        kv = h // (H // Hkv)
+        o_ref, lse_ref = oracle.full_attention(head_slice(q, h), head_slice(k, kv), head_slice(v, kv), causal=True,
+                                               cu_seqlens=cu)
+        assert_attention_close(o[:, :, h:h + 1].cpu().numpy(), o_ref, lse[:, h:h + 1].cpu().numpy(), lse_ref,
+                               "32K GQA packed %s, head %d, every row" % (layout, h))
