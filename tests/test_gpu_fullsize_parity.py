@@ -12,8 +12,10 @@ token-order sweep, ``RA_FLAG_SEQ_ORDER``):
     slices (4/64 of O);
   * the USP workload (L=262144, U=2 x R=4 zigzag): one head over windows of
     4096 rows on both sides of every zigzag-chunk / Ulysses-piece boundary (the
-    two coincide in token order), and the last 4096 rows (64K of 256K rows of
-    that head);
+    two coincide in token order), and the last 4096 rows (61440 of the head's
+    262144 rows);
+  * 32K with grouped key/value heads and packed sequences: two whole heads,
+    striped (the tile-skipping variant) and zigzag;
 
 and the pages' per-step structure at the 128K size ("From Ring Attention to
 DeepSpeed Ulysses to USP", jsqmd.com/news/734632, §3.1-§3.3: N rounds of block
