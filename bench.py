@@ -577,6 +577,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--config", type=int, default=None, choices=range(1, len(WORKLOADS) + 1),
+                    help="select the workload by its number, 1-5 (tiny non-causal, causal 8K, zigzag 2x32K, "
+                         "striped 128K, USP 256K); overrides --workload")
     ap.add_argument("--layout", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -599,6 +602,8 @@ def main():
                     help="B,L,H,d,N override of the workload's sizes (a smaller case for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.config is not None:
+        args.workload = list(WORKLOADS)[args.config - 1]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
