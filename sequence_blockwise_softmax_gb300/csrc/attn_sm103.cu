@@ -639,8 +639,8 @@ __global__ void __launch_bounds__(384, 1)
         // ================================================= softmax
         regs_grow<216>();
         if (TWO_ISSUERS && warp == 4) {
-            // the number of key tiles of the walk (one step at a time), for the
-            // two MMA issuers, counted while S(0) is being computed.  The
+            // the number of key tiles of the walk, one ring step per lane, for
+            // the two MMA issuers (the S issuer waits for it before S(0)).  The
             // tile-skipping variant also writes the step table: for each ring
             // step (one lane per step) the unit's key-tile range and each Q
             // tile's own range inside it, from its first row's sequence start
@@ -683,10 +683,12 @@ __global__ void __launch_bounds__(384, 1)
                     T += cnt;
                 }
             } else {
-                TileWalk w = walk0;
-                for (w.start_step(); w.valid(); w.start_step()) {
-                    T += w.tile_end - w.tile;
-                    ++w.step;
+                // one lane per ring step, summed over the warp
+                for (int s0 = 0; s0 < args.num_steps; s0 += 32) {
+                    int cnt = s0 + lane < args.num_steps ? walk0.step_tiles(s0 + lane) : 0;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+                    T += cnt;
                 }
             }
             __syncwarp();

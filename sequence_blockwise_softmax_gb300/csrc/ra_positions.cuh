@@ -100,6 +100,14 @@ struct TileWalk {
         }
     }
     RA_HD_STEP bool valid() const { return step < num_steps; }
+    // The number of key tiles step s visits (0 when its shard has no visible
+    // key): what start_step finds for that step, without walking to it.
+    RA_HD int step_tiles(int s) const {
+        const int js = kv_fixed >= 0 ? kv_fixed : ((q_rank - s - step_base) % N + N) % N;
+        const int t0 = (int)(keys_upto(layout, js, lo_pos, N, S) / 128);
+        const int t1 = (int)((keys_upto(layout, js, hi_pos, N, S) + 127) / 128);
+        return t1 > t0 ? t1 - t0 : 0;
+    }
     RA_HD_STEP void next() {
         if (++tile >= tile_end) {
             ++step;

@@ -45,8 +45,12 @@ void record_unit(Recorder &rc, int layout, int causal, const int *cu, int n_seqs
         ra::row_key_bounds(cu, n_seqs, total, ra::token_pos(layout, q_rank, gvalid[g] ? lrow : 0, N, S), causal,
                            unused, ghi[g]);
     }
+    // the per-step tile counts the forward's issuers are given agree with the walk
+    int visited = 0, counted = 0;
+    for (int s = 0; s < num_steps; ++s) counted += walk0.step_tiles(s);
     ra::TileWalk w = walk0;
     for (w.start_step(); w.valid(); w.next()) {
+        ++visited;
         int e[6];
         if (have_tab) ra::step_tile_ranges(layout, N, S, w.j, walk0.lo_pos, walk0.hi_pos, glo, ghi, gvalid, e);
         for (int a = row0; a < row_end; ++a) {
@@ -69,6 +73,7 @@ void record_unit(Recorder &rc, int layout, int causal, const int *cu, int n_seqs
             }
         }
     }
+    if (visited != counted) *rc.dup = 2;
 }
 
 }  // namespace
