@@ -26,6 +26,7 @@ counted).  Besides the device-resident number the JSON line carries:
 Under torchrun (N > 1) every rank runs its own replica of the workload.
 """
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -198,7 +199,14 @@ class Workload:
         if self.Hkv != H:
             # grouped-query attention: the first H_kv heads of the drawn K and V
             k, v = k[:, :, :self.Hkv].contiguous(), v[:, :, :self.Hkv].contiguous()
-        self.host = [t.pin_memory() for t in (q, k, v)]
+        with near_gpu(dev) as cpus:
+            self.host = [t.pin_memory() for t in (q, k, v)]
+            self.o_host = torch.empty((B, L, H, d), dtype=torch.float32).pin_memory()
+            self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
+            self.hosts_out = [(self.o_host, self.lse_host),
+                              (torch.empty_like(self.o_host).pin_memory(),
+                               torch.empty_like(self.lse_host).pin_memory())]
+        self.host_cpus = cpu_list(cpus) if cpus else None
         self.seq = [t.to(dev) for t in self.host]
         P = U * N
         self.heads = [H, self.Hkv, self.Hkv]
@@ -215,8 +223,6 @@ class Workload:
                         if U > 1 else None)
         self.o_seq = torch.empty((B, L, H, d), dtype=torch.float32, device=dev)
         self.lse_seq = torch.empty((B, H, L), dtype=torch.float32, device=dev)
-        self.o_host = torch.empty((B, L, H, d), dtype=torch.float32).pin_memory()
-        self.lse_host = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
         self.flags = ra.RA_FLAG_STEPWISE if stepwise else (ra.RA_FLAG_SEQ_ORDER if self.seq_order else 0)
         self.ws = ra.new_workspace(ra.ra_ring_attn_workspace_bytes(self.Bq, L, self.Hq, d, N, self.flags),
                                    device=dev)
@@ -356,14 +362,13 @@ class Workload:
         if not hasattr(self, "slots"):
             self.slots = [None, ([torch.empty_like(t) for t in self.seq], torch.empty_like(self.o_seq),
                                  torch.empty_like(self.lse_seq))]
-            self.hosts_out = [(self.o_host, self.lse_host),
-                              (torch.empty_like(self.o_host).pin_memory(),
-                               torch.empty_like(self.lse_host).pin_memory())]
             self.up, self.down = torch.cuda.Stream(), torch.cuda.Stream()
         compute = torch.cuda.current_stream()
         dev_bufs = [(self.seq, self.o_seq, self.lse_seq), self.slots[1]]
         Ev = lambda: torch.cuda.Event()
         up_done, comp_done, down_done = [Ev(), Ev()], [Ev(), Ev()], [Ev(), Ev()]
+        Tv = lambda: torch.cuda.Event(enable_timing=True)
+        copy_times = []          # per step: (upload start, end), (download start, end)
         barrier(world)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -376,8 +381,11 @@ class Workload:
             with torch.cuda.stream(self.up):
                 if i >= 2:
                     self.up.wait_event(comp_done[k])        # step i-2 has read these inputs
+                u0, u1 = Tv(), Tv()
+                u0.record(self.up)
                 for h, dbuf in zip(self.host, seq):
                     dbuf.copy_(h, non_blocking=True)
+                u1.record(self.up)
                 up_done[k].record(self.up)
             compute.wait_event(up_done[k])
             if i >= 2:
@@ -386,14 +394,23 @@ class Workload:
             comp_done[k].record(compute)
             with torch.cuda.stream(self.down):
                 self.down.wait_event(comp_done[k])
+                d0, d1 = Tv(), Tv()
+                d0.record(self.down)
                 self.hosts_out[k][0].copy_(o_seq, non_blocking=True)
                 self.hosts_out[k][1].copy_(lse_seq, non_blocking=True)
+                d1.record(self.down)
                 down_done[k].record(self.down)
+            copy_times.append(((u0, u1), (d0, d1)))
         compute.wait_stream(self.down)
         compute.wait_stream(self.up)
         e1.record(compute)
         torch.cuda.synchronize()
         barrier(world)
+        # the copy engines' rates (median over the steps), to read the end-to-end number by
+        up_ms = float(np.median([a.elapsed_time(b) for (a, b), _ in copy_times]))
+        down_ms = float(np.median([a.elapsed_time(b) for _, (a, b) in copy_times]))
+        self.copy_gbs = (self.h2d_bytes() / up_ms / 1e6 if up_ms > 0 else None,
+                         self.d2h_bytes() / down_ms / 1e6 if down_ms > 0 else None)
         return max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
 
     def h2d_bytes(self):
@@ -401,6 +418,58 @@ class Workload:
 
     def d2h_bytes(self):
         return self.o_host.numel() * 4 + self.lse_host.numel() * 4
+
+
+# ----------------------------------------------------------------- host memory
+def gpu_local_cpus(dev):
+    """The CPUs of the socket the GPU hangs off (sysfs local_cpulist of its PCI function),
+    limited to the ones this process may use; None when unknown."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        return (cpus & os.sched_getaffinity(0)) or None
+    except (OSError, AttributeError, ValueError):
+        return None
+
+
+@contextlib.contextmanager
+def near_gpu(dev):
+    """Pinned host buffers allocated inside are placed in the memory of the CPUs the GPU
+    is attached to (the process runs on those CPUs while the pages are pinned, then
+    returns to its own set), so that the step's copies do not cross sockets."""
+    cpus = gpu_local_cpus(dev)
+    saved = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        yield cpus
+    finally:
+        if cpus:
+            os.sched_setaffinity(0, saved)
+
+
+def cpu_list(cpus):
+    """'0-71' style text for a set of CPU numbers."""
+    out, run = [], []
+    for c in sorted(cpus):
+        if run and c == run[-1] + 1:
+            run.append(c)
+        else:
+            if run:
+                out.append("%d-%d" % (run[0], run[-1]) if len(run) > 1 else str(run[0]))
+            run = [c]
+    if run:
+        out.append("%d-%d" % (run[0], run[-1]) if len(run) > 1 else str(run[0]))
+    return ",".join(out)
 
 
 # ----------------------------------------------------------------- ring balance
@@ -691,7 +760,11 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": wl.h2d_bytes(),
                 "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": ms_e2e,
                 "copies": "every step uploads q/k/v and downloads O/LSE; two buffer slots, copies "
-                          "on their own streams overlap the neighbouring steps' compute"},
+                          "on their own streams overlap the neighbouring steps' compute",
+                "h2d_gbs": getattr(wl, "copy_gbs", (None, None))[0],
+                "d2h_gbs": getattr(wl, "copy_gbs", (None, None))[1],
+                "host_buffers": ("pinned, placed by the GPU's local CPUs %s" % wl.host_cpus if wl.host_cpus
+                                 else "pinned")},
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks.summary(),
     }
