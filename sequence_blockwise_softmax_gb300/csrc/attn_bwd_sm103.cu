@@ -14,10 +14,11 @@
 //                S^T = K Q^T and dP^T = V dO^T into tensor memory for each
 //                visible 128-query tile of every query rank and every query
 //                head of the group; the elementwise threads build P^T from
-//                S^T alone (bf16, into shared memory) and then dS^T once dP^T
-//                is there (bf16, back into tensor memory); dV += P^T dO and
-//                dK += dS^T Q accumulate in tensor memory.  With P^T in shared
-//                memory, S^T(t+1) only waits until S^T(t) is in registers, so
+//                S^T alone (bf16, into shared memory at d = 128, into free
+//                tensor-memory columns at d = 64) and then dS^T once dP^T is
+//                there (bf16, back into tensor memory); dV += P^T dO and
+//                dK += dS^T Q accumulate in tensor memory.  With P^T out of
+//                S^T's columns, S^T(t+1) only waits until S^T(t) is in registers, so
 //                P^T(t+1) can start as soon as dS^T(t) is done; dP^T(t+1)
 //                waits for dK(t), which reads the columns it overwrites.
 //   pass B       one CTA per 128 queries: S = Q K^T and dP = dO V^T for each
@@ -552,6 +553,13 @@ __global__ void __launch_bounds__(384, 1)
     using L = BwdKVSmem<D>;
     constexpr int NS = L::kStages;
     constexpr int HALVES = D / 64;
+    // At d = 64 S^T, dP^T, dV and dK leave tensor-memory columns 384-511
+    // free, so P^T goes there (queries 0-63 packed in 384-415, 64-127 in
+    // 416-447) and dV reads it as the A operand of a TS product: no P^T
+    // stores through shared memory and no proxy fence.  At d = 128 the four
+    // accumulators fill all 512 columns and P^T goes through shared memory.
+    constexpr bool PT_IN_TMEM = D == 64;
+    constexpr uint32_t kColPT = 384;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if ((smem_u32(smem) & 1023u) != 0u) {
@@ -728,11 +736,14 @@ __global__ void __launch_bounds__(384, 1)
                 if (!(ok = warp_wait(BAR(B_QFULL + st), (t / NS) & 1, abort_flag))) break;
                 if (!(ok = warp_wait(BAR(B_PFULL), t & 1, abort_flag))) break;
                 tc_fence_after();
-                issue_ss_half<D, 0>(tmem + 256, dp_k, ddo_mn + soff, t == 0);          // dV += P^T dO
+                // dV += P^T dO
+                if constexpr (PT_IN_TMEM) issue_ts_half<D, 0>(tmem + 256, tmem + kColPT, ddo_mn + soff, t == 0);
+                else issue_ss_half<D, 0>(tmem + 256, dp_k, ddo_mn + soff, t == 0);
                 __syncwarp();
                 if (!(ok = warp_wait(BAR(B_PFULL2), t & 1, abort_flag))) break;
                 tc_fence_after();
-                issue_ss_half<D, 1>(tmem + 256, dp_k, ddo_mn + soff, false);
+                if constexpr (PT_IN_TMEM) issue_ts_half<D, 1>(tmem + 256, tmem + kColPT, ddo_mn + soff, false);
+                else issue_ss_half<D, 1>(tmem + 256, dp_k, ddo_mn + soff, false);
                 tc_commit_elect(BAR(B_DVDONE));
                 __syncwarp();
                 if (!(ok = warp_wait(BAR(B_DSFULL), t & 1, abort_flag))) break;
@@ -821,19 +832,25 @@ __global__ void __launch_bounds__(384, 1)
                     pk[j][c >> 1] = pack_bf16x2(ex2(x0), ex2(x1));
                 }
             }
-            // P^T(t) goes to shared memory (the K-major A operand of dV, in the
-            // 128-byte-swizzled layout a TMA box load would give: 16-byte chunk
-            // j of row r at chunk j ^ (r mod 8)) once dV(t-1) has read P^T(t-1)
+            // P^T(t) goes where dV reads it once dV(t-1) has read P^T(t-1): at
+            // d = 64 to tensor memory (query 2c and 2c + 1 of the half in column c,
+            // the first in the low half), at d = 128 to shared memory (the K-major
+            // A operand of dV, in the 128-byte-swizzled layout a TMA box load would
+            // give: 16-byte chunk j of row r at chunk j ^ (r mod 8))
             if (t > 0 && !(ok = warp_wait(BAR(B_DVDONE), (t - 1) & 1, abort_flag))) break;
-            {
+            if constexpr (PT_IN_TMEM) {
+                tmem_st32(tmem + lane_off + kColPT + 32 * hh, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0][0]));
+                tmem_wait_st();
+                tc_fence_before();
+            } else {
                 uint8_t *prow = smem + L::kP + hh * L::kBox + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
                     *reinterpret_cast<uint4 *>(prow + ((jj ^ (r & 7)) << 4)) =
                         make_uint4(pk[jj >> 2][(jj & 3) * 4], pk[jj >> 2][(jj & 3) * 4 + 1],
                                    pk[jj >> 2][(jj & 3) * 4 + 2], pk[jj >> 2][(jj & 3) * 4 + 3]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(BAR(hh == 0 ? B_PFULL : B_PFULL2));
             // phase 2: dS^T = P^T (dP^T - D), 32 columns at a time
             if (!(ok = warp_wait(BAR(B_DPFULL), t & 1, abort_flag))) break;
