@@ -424,6 +424,8 @@ class Workload:
 def gpu_local_cpus(dev):
     """The CPUs of the socket the GPU hangs off (sysfs local_cpulist of its PCI function),
     limited to the ones this process may use; None when unknown."""
+    if getattr(dev, "type", None) != "cuda" or not torch.cuda.is_available():
+        return None
     try:
         p = torch.cuda.get_device_properties(dev)
         bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
@@ -437,7 +439,7 @@ def gpu_local_cpus(dev):
             elif part:
                 cpus.add(int(part))
         return (cpus & os.sched_getaffinity(0)) or None
-    except (OSError, AttributeError, ValueError):
+    except (OSError, AttributeError, ValueError, RuntimeError):
         return None
 
 

@@ -48,3 +48,16 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.job_value(3.518e13, 1, 30.0) == pytest.approx(1172.67, rel=1e-4)
+
+
+def test_host_buffer_placement_helpers():
+    """The e2e buffers' placement: CPU lists print compactly, and without a GPU (or its
+    sysfs entry) the placement leaves the process's CPU set untouched."""
+    import bench
+    assert bench.cpu_list({0, 1, 2, 3, 5, 7, 8, 9}) == "0-3,5,7-9"
+    assert bench.cpu_list({4}) == "4"
+    before = os.sched_getaffinity(0)
+    with bench.near_gpu(torch.device("cpu")) as cpus:
+        assert cpus is None
+        assert os.sched_getaffinity(0) == before
+    assert os.sched_getaffinity(0) == before
