@@ -174,27 +174,71 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const uint16_t *dout, cons
                                                       int N, int B, const float *lse_tok, float *lse_stack) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    constexpr int PER = D / 32;   // elements per lane
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-        const int64_t h = r % H, zs = r / H;
-        const int64_t s = zs % S, z = zs / S;
-        int64_t src = r, at_tok = 0;
-        if (seq_order) {
-            const int rank = (int)(z / B), b = (int)(z % B);
-            const int64_t p = token_pos(layout, rank, s, N, S);
-            src = ((int64_t)b * N * S + p) * H + h;
-            at_tok = ((int64_t)b * H + h) * N * S + p;
+    constexpr int PER = D / 32;   // elements per lane: one 8-byte (d = 128) or 4-byte dO load, one 16- or 8-byte O load
+    constexpr int R = 4;          // rows per warp and iteration
+    static_assert(PER == 2 || PER == 4, "d is 64 or 128");
+    // R rows per warp and iteration: every row's dO and O loads, and (lane u
+    // for row u) its LSE load, are issued before any reduction, so that one
+    // memory round trip serves R rows.
+    for (int64_t r0 = R * ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)); r0 < rows;
+         r0 += R * warps) {
+        int64_t dst[R];
+        uint32_t dw[R][PER / 2];
+        float ov[R][PER];
+        float my_lse = 0.f;   // lane u < R: the LSE of row u
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int64_t r = r0 + u;
+            dst[u] = -1;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) ov[u][e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < PER / 2; ++e) dw[u][e] = 0u;
+            if (r >= rows) continue;
+            const int64_t h = r % H, zs = r / H;
+            const int64_t s = zs % S, z = zs / S;
+            int64_t src = r;
+            if (seq_order) {
+                const int rank = (int)(z / B), b = (int)(z % B);
+                const int64_t p = token_pos(layout, rank, s, N, S);
+                src = ((int64_t)b * N * S + p) * H + h;
+                if (lane == u) my_lse = lse_tok[((int64_t)b * H + h) * N * S + p];
+            }
+            dst[u] = (z * H + h) * S + s;
+            const uint16_t *dp = dout + src * D + lane * PER;
+            const float *op = o + src * D + lane * PER;
+            if constexpr (PER == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(dp);
+                const float4 f = *reinterpret_cast<const float4 *>(op);
+                dw[u][0] = w.x;
+                dw[u][1] = w.y;
+                ov[u][0] = f.x;
+                ov[u][1] = f.y;
+                ov[u][2] = f.z;
+                ov[u][3] = f.w;
+            } else {
+                dw[u][0] = *reinterpret_cast<const uint32_t *>(dp);
+                const float2 f = *reinterpret_cast<const float2 *>(op);
+                ov[u][0] = f.x;
+                ov[u][1] = f.y;
+            }
         }
-        const uint16_t *dp = dout + src * D + lane * PER;
-        const float *op = o + src * D + lane * PER;
-        float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc += __uint_as_float((uint32_t)dp[e] << 16) * op[e];
+        for (int u = 0; u < R; ++u) {
+            // bf16 widened exactly (element 2k is the low half of word k),
+            // accumulated in element order
+            float acc = 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            dvec[(z * H + h) * S + s] = acc;
-            if (seq_order) lse_stack[(z * H + h) * S + s] = lse_tok[at_tok];
+            for (int e = 0; e < PER; ++e) {
+                const uint32_t w = dw[u][e >> 1];
+                acc += __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16)) * ov[u][e];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (dst[u] >= 0) {
+                if (lane == 0) dvec[dst[u]] = acc;
+                if (seq_order && lane == u) lse_stack[dst[u]] = my_lse;
+            }
         }
     }
 }
@@ -970,7 +1014,7 @@ static ra_status bwd_launch_t(const BwdLaunch &a, BwdArgs args, cudaStream_t str
         int dev = 0, sms = 148;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        int64_t blocks = (rows + 7) / 8;
+        int64_t blocks = (rows + 31) / 32;   // 8 warps of 4 rows
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
         bwd_dot_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(a.dout), a.o,
                                                                  a.dvec, rows, (int)a.H, a.S, a.seq_order ? 1 : 0,
