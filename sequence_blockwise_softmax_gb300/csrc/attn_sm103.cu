@@ -34,7 +34,8 @@
 //               (d = 128) or tensor memory (d = 64), O rescaled in place when
 //               the reference point moves,
 //               and the final normalisation, with O staged in shared memory
-//               for TMA stores.
+//               for TMA stores.  At d = 128 warp 4 first counts the unit's
+//               key tiles for the two issuers, one ring step per lane.
 // Tensor memory (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d), and at d = 64 P_0 [384, 448),
 // P_1 [448, 512) (bf16 pairs), which PV reads from there; at d = 128 P goes
